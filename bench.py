@@ -1,0 +1,348 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 dense fp16 GEMM, C = A @ B.T (K-major operands).
+
+One step = one C = A @ B.T over the whole workload (default: M = N = K = 8192,
+fp32 accumulation, fp16 output), inputs resident in HBM.  Prints ONE JSON line
+with TFLOP/s = 2*M*N*K / t, the roofline of the GEMM kernel against the
+measured dense tensor peak, an end-to-end number through the host-buffer
+entry point (host<->device copies inside the timed region), and the CPU
+oracle timed on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--acc f32|f16]
+
+--impl reference times the CPU oracle (the plain fp64 triple loop), on the
+host cores, on bounded row samples of the same workload.  For N > 1 (launched
+under torch.distributed.run) every rank runs an independent replica of the
+workload on its own GPU: the GEMM has no exchange step, so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+import gemm_workloads as wl
+
+METRIC = "fp16 GEMM TFLOP/s (2MNK/t) and % of GB300 dense fp16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_TFLOPS = 1900.0   # used only when the measured-peaks file is absent
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="gemm_8192", choices=list(wl.WORKLOADS))
+    p.add_argument("--acc", default="f32", choices=["f32", "f16"])
+    p.add_argument("--variant", default=None, help="force a kernel variant by name")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-rows", type=int, default=0,
+                   help="oracle sample size in rows (0 = sized for ~10 s)")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        # fp16 and bf16 dense tensor rates are nominally equal (1:1)
+        return {"tflops": float(d["bf16_tflops"]), "tflops_sustained":
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"tflops": FALLBACK_TFLOPS, "tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        self.out.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.out if ln.strip()]
+        os.unlink(self.out.name)
+        sm, mx, reasons, power = [], 0.0, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, r[5:9]):
+                if flag.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        # under load = samples above the idle floor
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def cpu_oracle_rate(w, rows_req=0, steps=1, a=None, b=None):
+    """Time the CPU oracle on `rows` seeded rows of the workload; returns
+    (TFLOP/s, threads used, sample description, seconds per step list)."""
+    import oracle
+    if a is None:
+        a, b = wl.inputs_for(w)
+    if rows_req <= 0:
+        # size the sample for about 10 s on this host: probe 8 rows first
+        probe = wl.sample_indices(w.M, 8, 99)
+        t0 = time.perf_counter()
+        oracle.gemm_rows_f64(a, b, probe)
+        per_row = (time.perf_counter() - t0) / len(probe)
+        rows_req = int(max(16, min(w.M, 10.0 / max(per_row, 1e-9))))
+    rows = wl.sample_indices(w.M, rows_req, 4242)
+    times, used = [], 0
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        _, used = oracle.gemm_rows_f64(a, b, rows, return_threads=True)
+        times.append(time.perf_counter() - t0)
+    flops = 2.0 * len(rows) * w.N * w.K
+    rate = flops / statistics.median(times) / 1e12
+    sample = (f"{len(rows)} seeded rows of C ({len(rows)}x{w.N}, K={w.K}) of {w.name}, "
+              f"fp64 triple loop")
+    return rate, used, sample, times
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = wl.WORKLOADS[args.workload]
+    a, b = wl.inputs_for(w)
+    # each step: a bounded row sample sized so warmup+steps end in a few minutes
+    budget_s = 150.0
+    nsteps = args.steps + args.warmup
+    probe = wl.sample_indices(w.M, 8, 99)
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gemm_rows_f64(a, b, probe)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    rows = int(max(8, min(w.M, budget_s / max(nsteps, 1) / max(per_row, 1e-9))))
+    if args.cpu_rows > 0:
+        rows = args.cpu_rows
+    if args.warmup:
+        cpu_oracle_rate(w, rows, steps=args.warmup, a=a, b=b)
+    rate, used, sample, times = cpu_oracle_rate(w, rows, steps=args.steps, a=a, b=b)
+    ms = statistics.median(times) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.describe()}", "acc": args.acc,
+                   "sample": sample},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import dense_fp16_gemm_04_gb300 as g
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    g.build()
+    plan = g.Plan(local)
+    if args.variant:
+        plan.set_variant(args.variant)
+    w = wl.WORKLOADS[args.workload]
+    a_np, b_np = wl.inputs_for(w)
+    a = torch.from_numpy(a_np).to(dev)
+    b = torch.from_numpy(b_np).to(dev)
+    c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    aptr, bptr, cptr = a.data_ptr(), b.data_ptr(), c.data_ptr()
+
+    def step():
+        plan.run_ptr(aptr, bptr, cptr, w.M, w.N, w.K, args.acc, sh)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    plan.check_error()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ----------------------------------------------------- device-timed run --
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = plan.launch_count
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
+    sampler = ClockSampler(gpu_index)
+    barrier()
+    with sampler:
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_all1.record(stream)
+        barrier()
+    launches = plan.launch_count - launches0
+    plan.check_error()
+    total_ms = t_all0.elapsed_time(t_all1)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = sampler.summary()
+
+    flops = float(w.flops)
+    value = world * args.steps * flops / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / args.steps
+    peaks = measured_peaks()
+    kernel_ms = statistics.mean(per_launch_ms)
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+
+    # ------------------------------------------------- end to end, host API --
+    e2e = None
+    if not args.no_e2e:
+        ha = torch.from_numpy(a_np).pin_memory()
+        hb = torch.from_numpy(b_np).pin_memory()
+        hc = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+        hp = (ha.data_ptr(), hb.data_ptr(), hc.data_ptr())
+        for _ in range(2):
+            plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)
+        e_steps = max(3, min(args.steps, 10))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)
+        dt = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([dt], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * e_steps * flops / dt / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(a_np.nbytes + b_np.nbytes),
+               "d2h_bytes_per_step": int(w.M * w.N * 2),
+               "ms_per_step": dt / e_steps * 1e3, "steps": e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, used, sample, _ = cpu_oracle_rate(w, args.cpu_rows, steps=1, a=a_np, b=b_np)
+        cpu = {"value": rate, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample}
+
+    traffic = _recorded_traffic(w.name, args.acc, plan.pick_variant(w.M, w.N, w.K, args.acc)[0])
+    variant, grid = plan.pick_variant(w.M, w.N, w.K, args.acc)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.describe()}", "M": w.M, "N": w.N, "K": w.K,
+                   "acc": args.acc, "variant": variant, "grid_ctas": grid,
+                   "l2": "inputs larger than L2 (A+B = %d MB vs 129 MB L2), no flush"
+                         % ((a_np.nbytes + b_np.nbytes) >> 20),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_peak": value / world / peaks["tflops"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["tflops"],
+                     "traffic": traffic, "peak_source": peaks["source"] + " bf16 burst (fp16 1:1)"},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _recorded_traffic(workload, acc, variant):
+    """DRAM bytes per launch from the committed ncu summary of this exact
+    kernel variant and workload, or None if none was recorded."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    return d.get(f"{variant}/{workload}/{acc}")
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

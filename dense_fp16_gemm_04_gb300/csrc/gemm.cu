@@ -1,0 +1,395 @@
+// gemm.cu -- host side of the C ABI declared in include/gemm.h: argument
+// checks, plans, tensor-map encoding and kernel launch for the sm_103a GEMM
+// C = A x B^T (tilus "A Minimal Hopper Matmul", section "Block Tiling").
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "gemm.h"
+#include "gemm_kernel.cuh"
+
+#define GB300_GEMM_VERSION "0.1.0"
+
+namespace {
+
+using gb300::CfgSingle;
+using gb300::GemmArgs;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// ------------------------------------------------------------ the variants --
+// Compile-time tile configurations; the host picks one per call.
+using SingleF32 = CfgSingle<256, 4, false>;
+using SingleF16 = CfgSingle<256, 4, true>;
+
+struct VariantInfo {
+  const char* name;
+  int tile_m, tile_n;  // output tile owned by one CTA
+};
+
+constexpr int kNumVariants = 1;
+constexpr VariantInfo kVariants[kNumVariants] = {
+    {"tc_single_128x256_s4", 128, 256},
+};
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s for any single wait
+constexpr int kGroupM = 8;                             // raster group height, tiles
+constexpr int kMapCacheSize = 16;
+
+struct MapEntry {
+  const void* ptr;
+  uint64_t rows, cols;
+  uint32_t box_rows, box_cols;
+  uint64_t stamp;
+  CUtensorMap map;
+};
+
+}  // namespace
+
+struct gemm_plan_s {
+  int device = 0;
+  int num_sms = 0;
+  EncodeTiledFn encode = nullptr;
+  uint32_t* d_err = nullptr;  // 4-word watchdog record
+  uint32_t last_err[4] = {0, 0, 0, 0};
+  uint64_t timeout_ns = kDefaultTimeoutNs;
+  int32_t skip_kb = -1;
+  int32_t forced_variant = -1;
+  uint64_t launches = 0;
+  uint64_t clock = 0;
+  MapEntry maps[kMapCacheSize];
+  // device staging for gemm_run_host
+  void* dA = nullptr;
+  void* dB = nullptr;
+  void* dC = nullptr;
+  size_t capA = 0, capB = 0, capC = 0;
+};
+
+namespace {
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+bool get_map(gemm_plan_s* p, CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols,
+             uint32_t box_rows, uint32_t box_cols) {
+  MapEntry* victim = &p->maps[0];
+  for (int i = 0; i < kMapCacheSize; ++i) {
+    MapEntry& e = p->maps[i];
+    if (e.stamp && e.ptr == ptr && e.rows == rows && e.cols == cols && e.box_rows == box_rows &&
+        e.box_cols == box_cols) {
+      e.stamp = ++p->clock;
+      *out = e.map;
+      return true;
+    }
+    if (e.stamp < victim->stamp) victim = &e;
+  }
+  // Row-major fp16 [rows, cols]: dimension 0 is the contiguous one.
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = p->encode(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr),
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    victim->stamp = 0;
+    return false;
+  }
+  victim->ptr = ptr;
+  victim->rows = rows;
+  victim->cols = cols;
+  victim->box_rows = box_rows;
+  victim->box_cols = box_cols;
+  victim->stamp = ++p->clock;
+  *out = victim->map;
+  return true;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Shape and enum checks shared by gemm_run and gemm_run_host.
+gemm_status_t check_shape(int64_t M, int64_t N, int64_t K, gemm_acc_t acc) {
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+  if (acc != GEMM_ACC_F32 && acc != GEMM_ACC_F16) return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (K % 8 != 0 || N % 8 != 0) return GEMM_ERR_ALIGNMENT;
+  return GEMM_OK;
+}
+
+int pick_variant(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, int* grid) {
+  int v = p->forced_variant >= 0 ? p->forced_variant : 0;
+  const VariantInfo& vi = kVariants[v];
+  const int64_t tiles = ((M + vi.tile_m - 1) / vi.tile_m) * ((N + vi.tile_n - 1) / vi.tile_n);
+  (void)K;
+  if (grid) *grid = static_cast<int>(tiles < p->num_sms ? tiles : p->num_sms);
+  return v;
+}
+
+template <class Cfg>
+cudaError_t launch_single(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                          const GemmArgs& args, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, gb300::gemm_tc_single<Cfg>, a, b, c, args);
+}
+
+gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, int64_t M,
+                         int64_t N, int64_t K, gemm_acc_t acc, cudaStream_t stream) {
+  if (K == 0) {
+    const int64_t n16 = M * N * 2 / 16;
+    const int64_t blocks = (n16 + 255) / 256;
+    gb300::gemm_zero_fill<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0,
+                            stream>>>(static_cast<uint4*>(C), n16);
+    ++p->launches;
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+  int grid = 0;
+  const int v = pick_variant(p, M, N, K, &grid);
+  const VariantInfo& vi = kVariants[v];
+  CUtensorMap ma, mb, mc;
+  if (!get_map(p, &ma, A, M, K, vi.tile_m, 64) || !get_map(p, &mb, B, N, K, vi.tile_n, 64) ||
+      !get_map(p, &mc, C, M, N, 32, 64))
+    return GEMM_ERR_CUDA;
+
+  GemmArgs args;
+  args.M = static_cast<int32_t>(M);
+  args.N = static_cast<int32_t>(N);
+  args.K = static_cast<int32_t>(K);
+  args.tiles_m = static_cast<int32_t>((M + vi.tile_m - 1) / vi.tile_m);
+  args.tiles_n = static_cast<int32_t>((N + vi.tile_n - 1) / vi.tile_n);
+  args.num_kb = static_cast<int32_t>((K + 63) / 64);
+  args.num_tiles = args.tiles_m * args.tiles_n;
+  args.group_m = kGroupM;
+  args.err = p->d_err;
+  args.timeout_ns = p->timeout_ns;
+  args.skip_kb = p->skip_kb;
+
+  cudaError_t e = acc == GEMM_ACC_F32 ? launch_single<SingleF32>(ma, mb, mc, args, grid, stream)
+                                      : launch_single<SingleF16>(ma, mb, mc, args, grid, stream);
+  ++p->launches;
+  return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+template <class Cfg>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(gb300::gemm_tc_single<Cfg>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+}
+
+gemm_status_t grow(void** buf, size_t* cap, size_t need) {
+  if (need <= *cap) return GEMM_OK;
+  if (*buf) cudaFree(*buf);
+  *buf = nullptr;
+  *cap = 0;
+  if (cudaMalloc(buf, need) != cudaSuccess) {
+    *buf = nullptr;
+    return GEMM_ERR_OOM;
+  }
+  *cap = need;
+  return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gemm_version(void) { return GB300_GEMM_VERSION; }
+
+const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+    case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    case GEMM_ERR_OOM: return "GEMM_ERR_OOM";
+  }
+  return "GEMM_ERR_UNKNOWN";
+}
+
+int32_t gemm_variant_count(void) { return kNumVariants; }
+
+const char* gemm_variant_name(int32_t v) {
+  return (v >= 0 && v < kNumVariants) ? kVariants[v].name : nullptr;
+}
+
+gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (device < 0 || device >= ndev) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
+
+  gemm_plan_s* p = new (std::nothrow) gemm_plan_s();
+  if (!p) return GEMM_ERR_OOM;
+  std::memset(p->maps, 0, sizeof(p->maps));
+  p->device = device;
+  p->num_sms = sms;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    delete p;
+    return GEMM_ERR_CUDA;
+  }
+  p->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  if (set_smem_attr<SingleF32>() != cudaSuccess || set_smem_attr<SingleF16>() != cudaSuccess) {
+    delete p;
+    return GEMM_ERR_CUDA;
+  }
+  if (cudaMalloc(&p->d_err, 4 * sizeof(uint32_t)) != cudaSuccess) {
+    delete p;
+    return GEMM_ERR_OOM;
+  }
+  if (cudaMemset(p->d_err, 0, 4 * sizeof(uint32_t)) != cudaSuccess) {
+    cudaFree(p->d_err);
+    delete p;
+    return GEMM_ERR_CUDA;
+  }
+  *out = p;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_destroy(gemm_plan_t p) {
+  if (!p) return GEMM_OK;
+  DeviceGuard g(p->device);
+  if (p->d_err) cudaFree(p->d_err);
+  if (p->dA) cudaFree(p->dA);
+  if (p->dB) cudaFree(p->dB);
+  if (p->dC) cudaFree(p->dC);
+  delete p;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_watchdog(gemm_plan_t p, uint64_t timeout_ns, int32_t skip_k_block) {
+  if (!p || skip_k_block < -1) return GEMM_ERR_INVALID_ARG;
+  p->timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+  p->skip_kb = skip_k_block;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_variant(gemm_plan_t p, int32_t v) {
+  if (!p || v < -1 || v >= kNumVariants) return GEMM_ERR_INVALID_ARG;
+  p->forced_variant = v;
+  return GEMM_OK;
+}
+
+int32_t gemm_plan_pick_variant(gemm_plan_t p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
+                               int32_t* grid_ctas) {
+  if (!p || check_shape(M, N, K, acc) != GEMM_OK) return -1;
+  int grid = 0;
+  int v = pick_variant(p, M, N, K, &grid);
+  if (grid_ctas) *grid_ctas = grid;
+  return v;
+}
+
+uint64_t gemm_plan_launch_count(gemm_plan_t p) { return p ? p->launches : 0; }
+
+gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, int64_t M, int64_t N,
+                       int64_t K, gemm_acc_t acc, void* stream) {
+  if (!p) return GEMM_ERR_INVALID_ARG;
+  gemm_status_t s = check_shape(M, N, K, acc);
+  if (s != GEMM_OK) return s;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(C) & 15) ||
+      (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))))
+    return GEMM_ERR_ALIGNMENT;
+  const size_t bytesC = static_cast<size_t>(M) * N * 2;
+  if (K > 0 && (overlaps(C, bytesC, A, static_cast<size_t>(M) * K * 2) ||
+                overlaps(C, bytesC, B, static_cast<size_t>(N) * K * 2)))
+    return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  return run_device(p, A, B, C, M, N, K, acc, static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_plan_check_error(gemm_plan_t p) {
+  if (!p) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  uint32_t rec[4] = {0, 0, 0, 0};
+  if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaMemcpy(rec, p->d_err, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (rec[0] == 0) return GEMM_OK;
+  std::memcpy(p->last_err, rec, sizeof(rec));
+  if (cudaMemset(p->d_err, 0, sizeof(rec)) != cudaSuccess) return GEMM_ERR_CUDA;
+  return static_cast<gemm_status_t>(rec[0]);
+}
+
+gemm_status_t gemm_plan_last_error_detail(gemm_plan_t p, uint32_t detail[4]) {
+  if (!p || !detail) return GEMM_ERR_INVALID_ARG;
+  std::memcpy(detail, p->last_err, sizeof(p->last_err));
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_run_host(gemm_plan_t p, const void* A, const void* B, void* C, int64_t M,
+                            int64_t N, int64_t K, gemm_acc_t acc, void* stream) {
+  if (!p) return GEMM_ERR_INVALID_ARG;
+  gemm_status_t s = check_shape(M, N, K, acc);
+  if (s != GEMM_OK) return s;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  const size_t bA = static_cast<size_t>(M) * K * 2, bB = static_cast<size_t>(N) * K * 2,
+               bC = static_cast<size_t>(M) * N * 2;
+  if ((s = grow(&p->dA, &p->capA, bA > 0 ? bA : 16)) != GEMM_OK) return s;
+  if ((s = grow(&p->dB, &p->capB, bB > 0 ? bB : 16)) != GEMM_OK) return s;
+  if ((s = grow(&p->dC, &p->capC, bC)) != GEMM_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K > 0) {
+    if (cudaMemcpyAsync(p->dA, A, bA, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(p->dB, B, bB, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+  }
+  s = run_device(p, p->dA, p->dB, p->dC, M, N, K, acc, st);
+  if (s != GEMM_OK) return s;
+  if (cudaMemcpyAsync(C, p->dC, bC, cudaMemcpyDeviceToHost, st) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GEMM_ERR_CUDA;
+  uint32_t code = 0;
+  if (cudaMemcpy(&code, p->d_err, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  return code == 0 ? GEMM_OK : gemm_plan_check_error(p);
+}
+
+}  // extern "C"

@@ -1,0 +1,361 @@
+// gemm_kernel.cuh -- persistent, warp-specialized tcgen05 GEMM for sm_103a.
+//
+//   C[M,N] = A[M,K] x B[N,K]^T, fp16 in, fp32 or fp16 accumulate, fp16 out
+//   (tilus "A Minimal Hopper Matmul", section "Block Tiling").
+//
+// One CTA per SM loops over output tiles (static stride over a grouped
+// raster).  Inside the CTA the work is split by warp, as in the producer /
+// consumer split of tilus "Warp Specialization", redesigned for tcgen05:
+//
+//   warp 0, lane 0   TMA producer: fills a kStages-deep ring of A/B k-blocks,
+//                    one "full" mbarrier (transaction bytes) per stage.
+//   warp 1           allocates tensor memory; lane 0 issues every tcgen05.mma
+//                    of the CTA and releases each stage with tcgen05.commit
+//                    onto its "empty" mbarrier.
+//   warps 2..5       epilogue: tcgen05.ld the accumulator, round to fp16,
+//                    stage through swizzled shared memory, TMA-store.
+//
+// The accumulator lives in tensor memory, double-buffered (2 x BN columns),
+// so the epilogue of tile i overlaps the main loop of tile i+1; two more
+// barrier pairs (tmem_full / tmem_empty) hand the buffers back and forth.
+//
+// Every wait is bounded: a wait that outlives the timeout records the site in
+// a device watchdog word, raises a CTA-wide abort flag, and every role then
+// leaves its loop; the CTA waits (again bounded) for its own loads and MMAs,
+// frees tensor memory and returns.
+#pragma once
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gb300 {
+
+// Where a wait gave up (reported in the watchdog record's second word).
+enum WaitSite : uint32_t {
+  kSiteEmpty = 1,      // producer waiting for a free stage
+  kSiteFull = 2,       // MMA issuer waiting for a filled stage
+  kSiteTmemEmpty = 3,  // MMA issuer waiting for a drained accumulator buffer
+  kSiteTmemFull = 4,   // epilogue waiting for a finished accumulator
+  kSiteMmaDone = 5,    // teardown: waiting for the last MMAs
+  kSiteDrain = 6,      // teardown: producer waiting for its last stages
+};
+
+constexpr uint32_t kStatusTimeout = 5;  // == GEMM_ERR_TIMEOUT
+
+struct GemmArgs {
+  int32_t M, N, K;
+  int32_t tiles_m, tiles_n, num_kb, num_tiles;
+  int32_t group_m;      // raster group height, in tiles
+  uint32_t* err;        // device watchdog record, 4 words
+  uint64_t timeout_ns;  // longest allowed single wait
+  int32_t skip_kb;      // fault injection, -1 = off
+};
+
+// Tile configuration of the single-CTA kernel.
+template <int kBN_, int kStages_, bool kAccF16_>
+struct CfgSingle {
+  static constexpr int kBM = 128, kBN = kBN_, kBK = 64, kStages = kStages_;
+  static constexpr bool kAccF16 = kAccF16_;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = kBN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 fp16, 128B swizzle
+  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kStages * kABytes;
+  static constexpr int kOffEpi = kStages * kStageBytes;
+  static constexpr int kOffBar = kOffEpi + kEpiBytes;
+  static constexpr int kNumBars = 2 * kStages + 5;  // full, empty, tmem_full[2], tmem_empty[2], mma_done
+  static constexpr int kOffSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffSlot + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
+  static constexpr int kTmemCols = 2 * kBN;
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kIdesc = ptx::idesc_f16(kBM, kBN, !kAccF16);
+
+  static_assert(kBN % 64 == 0 && kBN >= 64 && kBN <= 256, "BN must be 64..256 in steps of 64");
+  static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM columns: power of 2");
+  static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory per CTA");
+  static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1024 B alignment");
+  // Barriers sit after every TMA destination, never inside one (tilus "A
+  // Minimal Hopper Matmul", Epilogue note: a barrier placed inside a live TMA
+  // destination is silently corrupted).
+  static_assert(kOffBar >= kOffEpi + kEpiBytes, "barriers overlap a TMA buffer");
+};
+
+struct Watch {
+  volatile uint32_t* abort;
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+// Slow path of a bounded mbarrier wait.  Returns false when the wait gave up,
+// either because the CTA is aborting (and honor_abort) or after timeout_ns.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Watch w, uint32_t site,
+                                       int32_t tile, bool honor_abort) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *w.abort) return false;
+    if (ptx::globaltimer_ns() - t0 > w.timeout_ns) {
+      if (atomicCAS(w.err, 0u, kStatusTimeout) == 0u) {
+        w.err[1] = site;
+        w.err[2] = blockIdx.x;
+        w.err[3] = static_cast<uint32_t>(tile);
+      }
+      *w.abort = 1u;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Watch& w,
+                                         uint32_t site, int32_t tile, bool honor_abort = true) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, w, site, tile, honor_abort);
+}
+
+// Grouped raster: tiles are walked down a group of `group` tile-rows before
+// moving one tile-column right, so CTAs running at the same time share A rows
+// and B rows in L2.  A bijection of [0, tiles_m*tiles_n).
+__device__ __forceinline__ void raster(int32_t t, int32_t tiles_m, int32_t tiles_n, int32_t group,
+                                       int32_t& mb, int32_t& nb) {
+  const int32_t per = group * tiles_n;
+  const int32_t g = t / per;
+  const int32_t m0 = g * group;
+  const int32_t gs = min(group, tiles_m - m0);
+  const int32_t r = t - g * per;
+  mb = m0 + r % gs;
+  nb = r / gs;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    gemm_tc_single(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = ptx::smem_addr(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = sb + Cfg::kOffBar;
+  auto bar_full = [&](int s) { return bar0 + 8u * s; };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (S + s); };
+  auto bar_tfull = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto bar_tempty = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t bar_mma_done = bar0 + 8u * (2 * S + 4);
+  auto sA = [&](int s) { return sb + Cfg::kOffA + s * Cfg::kABytes; };
+  auto sB = [&](int s) { return sb + Cfg::kOffB + s * Cfg::kBBytes; };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
+  const Watch w{abort_flag, args.err, args.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmC);
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(bar_full(s), 1);
+      ptx::mbar_init(bar_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar_tfull(b), 1);
+      ptx::mbar_init(bar_tempty(b), Cfg::kEpiWarps);
+    }
+    ptx::mbar_init(bar_mma_done, 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc<1>(sb + Cfg::kOffSlot, Cfg::kTmemCols);
+    ptx::tmem_relinquish<1>();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffSlot);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer --
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t fills = 0;
+      bool ok = true;
+      for (int32_t tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+        int32_t mb, nb;
+        raster(tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
+        for (int32_t kb = 0; kb < args.num_kb; ++kb) {
+          if (!wait_bar(bar_empty(stage), phase ^ 1u, w, kSiteEmpty, tile)) {
+            ok = false;
+            break;
+          }
+          const bool skip = args.skip_kb == kb && tile == static_cast<int32_t>(blockIdx.x) &&
+                            blockIdx.x == 0;
+          if (!skip) {
+            ptx::mbar_arrive_expect_tx(bar_full(stage), Cfg::kStageBytes);
+            ptx::tma_load_2d(sA(stage), &tmA, bar_full(stage), kb * Cfg::kBK, mb * Cfg::kBM);
+            ptx::tma_load_2d(sB(stage), &tmB, bar_full(stage), kb * Cfg::kBK, nb * Cfg::kBN);
+          }
+          ++fills;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: the last min(S, fills) fills may still be in use.  Normally
+      // wait until the MMA issuer has released each of them, so no tcgen05
+      // arrival is still headed for the ring when the CTA exits (tilus "Warp
+      // Specialization", "Draining the Pipeline").  When aborting, wait
+      // instead (bounded, ignoring the abort flag) for those loads to land.
+      const int64_t n = fills < S ? fills : S;
+      for (int64_t f = fills - n; f < fills; ++f) {
+        const int s = static_cast<int>(f % S);
+        const uint32_t par = static_cast<uint32_t>((f / S) & 1);
+        if (ok)
+          ok = wait_bar(bar_empty(s), par, w, kSiteDrain, -1);
+        if (!ok) wait_bar(bar_full(s), par, w, kSiteDrain, -1, /*honor_abort=*/false);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer --
+      int stage = 0;
+      uint32_t phase = 0;
+      int32_t acc_iter = 0;
+      bool ok = true;
+      for (int32_t tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+        const int buf = acc_iter & 1;
+        const uint32_t use_par = static_cast<uint32_t>((acc_iter >> 1) & 1);
+        if (!wait_bar(bar_tempty(buf), use_par ^ 1u, w, kSiteTmemEmpty, tile)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kBN);
+        for (int32_t kb = 0; kb < args.num_kb; ++kb) {
+          if (!wait_bar(bar_full(stage), phase, w, kSiteFull, tile)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t a_desc = ptx::sw128_kmajor_desc(sA(stage));
+          const uint64_t b_desc = ptx::sw128_kmajor_desc(sB(stage));
+#pragma unroll
+          for (int k = 0; k < Cfg::kBK / 16; ++k) {
+            // +32 bytes along K per 16-element step, inside the swizzled row
+            ptx::mma_f16<1>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+                            (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(bar_empty(stage));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar_tfull(buf));
+        ++acc_iter;
+      }
+      // Every MMA this thread issued has finished before tensor memory is
+      // freed (bounded, whatever the abort state).
+      ptx::mma_commit(bar_mma_done);
+      wait_bar(bar_mma_done, 0u, w, kSiteMmaDone, -1, /*honor_abort=*/false);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    const int q = warp & 3;  // this warp may touch TMEM lanes 32q .. 32q+31 only
+    const uint32_t stage_base = sb + Cfg::kOffEpi + static_cast<uint32_t>(q * 2 * Cfg::kEpiBufBytes);
+    uint32_t stores = 0;
+    int32_t acc_iter = 0;
+    for (int32_t tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
+      int32_t mb, nb;
+      raster(tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
+      const int buf = acc_iter & 1;
+      const uint32_t use_par = static_cast<uint32_t>((acc_iter >> 1) & 1);
+      int ok = 1;
+      if (lane == 0) ok = wait_bar(bar_tfull(buf), use_par, w, kSiteTmemFull, tile) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(buf * Cfg::kBN);
+      const int32_t row0 = mb * Cfg::kBM + q * 32;
+#pragma unroll 1
+      for (int c = 0; c < Cfg::kBN / 64; ++c) {
+        uint32_t packed[32];
+        if constexpr (Cfg::kAccF16) {
+          ptx::tmem_ld_32x32b_x32_pack16(t_row + c * 64, packed);
+          ptx::tmem_wait_ld();
+        } else {
+          uint32_t v0[32], v1[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c * 64, v0);
+          ptx::tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            packed[i] = pack_half2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+            packed[16 + i] = pack_half2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+          }
+        }
+        if (c == Cfg::kBN / 64 - 1) {
+          // The whole accumulator buffer is in registers: hand it back.
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar_tempty(buf));
+        }
+        const uint32_t sbuf = stage_base + (stores & 1u) * Cfg::kEpiBufBytes;
+        if (stores >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();
+        __syncwarp();
+        // Row `lane` of the 32x64 staging tile, 16-byte chunk j stored at
+        // chunk position j ^ (row % 8): the 128-byte swizzle the C tensor
+        // map expects, and conflict-free across the warp.
+        const uint32_t row_addr = sbuf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          ptx::st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                            packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        const int32_t col0 = nb * Cfg::kBN + c * 64;
+        if (lane == 0 && row0 < args.M && col0 < args.N) {
+          ptx::tma_store_2d(&tmC, sbuf, col0, row0);
+          ptx::bulk_commit_group();
+          ++stores;
+        }
+        stores = __shfl_sync(0xffffffffu, stores, 0);
+      }
+      ++acc_iter;
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc<1>(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// C := 0 for K == 0 (the empty sum).  C rows are a multiple of 16 bytes.
+__global__ void gemm_zero_fill(uint4* c, int64_t n16) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    c[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+}  // namespace gb300

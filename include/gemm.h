@@ -1,0 +1,148 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense fp16 GEMM library.
+ *
+ * The operation (tilus "A Minimal Hopper Matmul", section "Block Tiling", and
+ * its note "Data layout: K-major"):
+ *
+ *     C[M, N] = A[M, K] x B[N, K]^T,    C[i][j] = sum_k A[i][k] * B[j][k]
+ *
+ * A, B and C are fp16 (IEEE binary16), row-major, K contiguous in A and B.
+ * The sum runs on the tensor cores (tcgen05.mma, accumulator in tensor
+ * memory), accumulated in fp32 (GEMM_ACC_F32) or natively in fp16
+ * (GEMM_ACC_F16, tilus "Four Consumers, FP16 Accumulation, and a TMA
+ * Epilogue", section "The Register Budget Problem"), and written as fp16
+ * rounded to nearest even.
+ *
+ * Ownership: the caller owns every buffer.  The library owns only the plan
+ * (a few bytes of device memory for the watchdog record, and, for
+ * gemm_run_host, device staging buffers it grows on demand).
+ *
+ * Errors: every entry point returns a gemm_status_t.  Argument checks run on
+ * the host before any launch, so a rejected call writes nothing.  A kernel
+ * that stops making progress (a wait that outlives the plan's timeout) does
+ * not hang: it records GEMM_ERR_TIMEOUT on the device, frees its tensor
+ * memory and returns; gemm_plan_check_error reports it.
+ *
+ * Threads: a plan may be used by one host thread at a time.  Different plans
+ * are independent.
+ */
+#ifndef GB300_GEMM_H_
+#define GB300_GEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_plan_s* gemm_plan_t;
+
+/* Accumulation precision inside the tensor cores. */
+typedef enum {
+    GEMM_ACC_F32 = 0, /* fp32 accumulate, fp16 output (the default) */
+    GEMM_ACC_F16 = 1  /* native fp16 accumulate, fp16 output */
+} gemm_acc_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,        /* null plan/pointer, negative or oversized dim, bad enum, C overlaps A or B */
+    GEMM_ERR_ALIGNMENT = 2,          /* pointer not 16-byte aligned, K or N not a multiple of 8 */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* device is not compute capability 10.3 (sm_103a) */
+    GEMM_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed (launch, copy, allocation of plan memory) */
+    GEMM_ERR_TIMEOUT = 5,            /* the kernel's watchdog fired: a wait outlived the plan's timeout */
+    GEMM_ERR_OOM = 6                 /* host or device memory for the plan could not be allocated */
+} gemm_status_t;
+
+/* Create a plan bound to CUDA device `device` (must be an sm_103 part).
+ * Queries the SM count, resolves the tensor-map encoder from the driver, sets
+ * the kernels' shared-memory limits and allocates the 16-byte device watchdog
+ * record.  *out receives the plan, or NULL on error. */
+GEMM_API gemm_status_t gemm_plan_create(gemm_plan_t* out, int device);
+
+/* Release the plan and everything it allocated.  NULL is accepted (no-op).
+ * Must not be called while work launched with the plan is still running. */
+GEMM_API gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
+
+/* C = A x B^T on device buffers, asynchronously on `stream` (a cudaStream_t;
+ * NULL = legacy default stream).
+ *   A : device pointer, fp16 [M, K] row-major (K contiguous), 16-byte aligned
+ *   B : device pointer, fp16 [N, K] row-major (K contiguous), 16-byte aligned
+ *   C : device pointer, fp16 [M, N] row-major, 16-byte aligned, must not
+ *       overlap A or B
+ *   M, N, K : 0 <= M, N, K <= 2^31 - 1;  K % 8 == 0 and N % 8 == 0 (every
+ *       row starts on a 16-byte boundary, as the tensor-memory-access engine
+ *       requires).  M == 0 or N == 0: nothing to do, GEMM_OK, pointers
+ *       unused.  K == 0: C is filled with +0 (the empty sum).
+ *   acc : GEMM_ACC_F32 or GEMM_ACC_F16.
+ * Allocates nothing, does not synchronize.  Launch failures return
+ * GEMM_ERR_CUDA; a device-side watchdog timeout surfaces later through
+ * gemm_plan_check_error. */
+GEMM_API gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C,
+                       int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
+                       void* stream);
+
+/* Same product on HOST buffers: copies A and B to device staging buffers owned
+ * by the plan (grown with cudaMalloc on first use of a larger shape), runs
+ * gemm_run on `stream`, copies C back and synchronizes `stream` before
+ * returning.  A, B, C are host pointers (pinned memory gives full copy
+ * bandwidth; pageable memory works but is slower).  Same shape and
+ * alignment rules as gemm_run (host pointers need no particular alignment).
+ * Returns the watchdog status of the run as well. */
+GEMM_API gemm_status_t gemm_run_host(gemm_plan_t plan, const void* A, const void* B, void* C,
+                            int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
+                            void* stream);
+
+/* Synchronize the plan's device, read and clear the watchdog record.
+ * Returns GEMM_OK, GEMM_ERR_TIMEOUT (the record is then described by
+ * gemm_plan_last_error_detail) or GEMM_ERR_CUDA if the context is broken. */
+GEMM_API gemm_status_t gemm_plan_check_error(gemm_plan_t plan);
+
+/* The last watchdog record read by gemm_plan_check_error:
+ * detail[0] = status code, detail[1] = which wait gave up (see the kernel's
+ * WaitSite list), detail[2] = CTA index, detail[3] = tile index. */
+GEMM_API gemm_status_t gemm_plan_last_error_detail(gemm_plan_t plan, uint32_t detail[4]);
+
+/* Watchdog and fault-injection controls (testing and diagnosis).
+ * timeout_ns: how long any one wait inside the kernel may take before it
+ *   gives up (default 2e9 ns; 0 restores the default).
+ * skip_k_block: -1 (default) for normal operation; a value >= 0 makes the
+ *   producer skip the load of that k-block of the first tile of CTA 0 and
+ *   never declare its bytes, so the consumer's wait for it can only end by
+ *   timing out.  Used to test that a stuck wait returns an error and leaves
+ *   the context usable. */
+GEMM_API gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout_ns,
+                                     int32_t skip_k_block);
+
+/* Override the kernel variant chosen for a shape (-1 = automatic).  The
+ * variants are listed by gemm_variant_name(0 .. gemm_variant_count()-1). */
+GEMM_API gemm_status_t gemm_plan_set_variant(gemm_plan_t plan, int32_t variant);
+GEMM_API int32_t gemm_variant_count(void);
+GEMM_API const char* gemm_variant_name(int32_t variant);
+
+/* The variant gemm_run would use for this shape and accumulation, and the
+ * grid it would launch (CTAs), or -1 on a rejected shape. */
+GEMM_API int32_t gemm_plan_pick_variant(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
+                               gemm_acc_t acc, int32_t* grid_ctas);
+
+/* Kernel launches issued through this plan so far (gemm_run and
+ * gemm_run_host; the K == 0 zero-fill counts as one). */
+GEMM_API uint64_t gemm_plan_launch_count(gemm_plan_t plan);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+GEMM_API const char* gemm_status_string(gemm_status_t s);
+
+/* Library version string (static storage). */
+GEMM_API const char* gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H_ */

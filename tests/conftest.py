@@ -46,3 +46,59 @@ def read_golden(name):
             scalars[parts[0]] = float(parts[1])
             i += 1
     return mats, scalars
+
+
+# ------------------------------------------------------------ GPU helpers --
+# Pass bounds on unit-variance outputs: fp32 accumulation |err| <= 1e-2 and
+# |err| / max(|ref|, 1) <= 1e-2; native fp16 accumulation |err| <= 5e-2 (the
+# bound tilus "Four Consumers, FP16 Accumulation, and a TMA Epilogue" uses for
+# its K=8192 fp16-accumulated check, "The Register Budget Problem").
+TOL = {"f32": (1e-2, 1e-2), "f16": (5e-2, None)}
+
+
+def error_stats(got, ref):
+    import numpy as np
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - ref)
+    rel = err / np.maximum(np.abs(ref), 1.0)
+    return {"max_abs": float(err.max()) if err.size else 0.0,
+            "mean_abs": float(err.mean()) if err.size else 0.0,
+            "p99_abs": float(np.percentile(err, 99)) if err.size else 0.0,
+            "max_rel": float(rel.max()) if rel.size else 0.0,
+            "finite": bool(np.isfinite(got).all())}
+
+
+def assert_close(got, ref, acc, what=""):
+    st = error_stats(got, ref)
+    atol, rtol = TOL[acc]
+    assert st["finite"], f"{what}: non-finite outputs"
+    assert st["max_abs"] <= atol, f"{what}: max |err| {st['max_abs']:.4g} > {atol} ({st})"
+    if rtol is not None:
+        assert st["max_rel"] <= rtol, f"{what}: max rel err {st['max_rel']:.4g} > {rtol}"
+    return st
+
+
+@pytest.fixture(scope="session")
+def plan():
+    import dense_fp16_gemm_04_gb300 as g
+    g.build()
+    p = g.Plan(0)
+    yield p
+    p.close()
+
+
+def to_dev(x):
+    import torch
+    return torch.from_numpy(x).cuda()
+
+
+def run_gpu(plan, a, b, acc="f32", fill=float("nan")):
+    """C = A @ B.T on the GPU through the C ABI; C is pre-filled with NaN so
+    any element the kernel fails to write shows up."""
+    import numpy as np
+    import torch
+    ta, tb = to_dev(a), to_dev(b)
+    c = torch.full((a.shape[0], b.shape[0]), fill, dtype=torch.float16, device="cuda")
+    plan.run(ta, tb, c, acc=acc)
+    plan.check_error()
+    return c.cpu().numpy()

@@ -1,0 +1,135 @@
+"""GPU edge cases: empty shapes, K == 0, argument rejection before any write,
+out-of-bounds canaries, repeated launches, streams, and the host-buffer entry
+point."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import dense_fp16_gemm_04_gb300 as g
+import gemm_workloads as wl
+import oracle
+from conftest import assert_close, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+OK, INVALID, ALIGN = 0, 1, 2
+
+
+def test_empty_M_or_N_is_a_no_op(plan):
+    c = torch.full((4, 8), 7.0, dtype=torch.float16, device="cuda")
+    a = torch.ones((4, 16), dtype=torch.float16, device="cuda")
+    before = plan.launch_count
+    assert plan.status_run(a.data_ptr(), a.data_ptr(), c.data_ptr(), 0, 8, 16) == OK
+    assert plan.status_run(a.data_ptr(), a.data_ptr(), c.data_ptr(), 4, 0, 16) == OK
+    assert plan.status_run(0, 0, 0, 0, 0, 0) == OK
+    torch.cuda.synchronize()
+    assert plan.launch_count == before
+    assert bool((c == 7.0).all())
+
+
+def test_K_zero_gives_zeros(plan):
+    c = torch.full((33, 40), float("nan"), dtype=torch.float16, device="cuda")
+    assert plan.status_run(0, 0, c.data_ptr(), 33, 40, 0) == OK
+    plan.check_error()
+    assert bool((c == 0).all())
+
+
+def test_rejected_arguments_write_nothing(plan):
+    a = torch.ones((64, 64), dtype=torch.float16, device="cuda")
+    b = torch.ones((64, 64), dtype=torch.float16, device="cuda")
+    c = torch.full((64, 64), 3.0, dtype=torch.float16, device="cuda")
+    pa, pb, pc = a.data_ptr(), b.data_ptr(), c.data_ptr()
+    assert plan.status_run(pa, pb, pc, 64, 64, 60) == ALIGN          # K % 8
+    assert plan.status_run(pa, pb, pc, 64, 60, 64) == ALIGN          # N % 8
+    assert plan.status_run(pa + 2, pb, pc, 64, 64, 64) == ALIGN      # misaligned A
+    assert plan.status_run(pa, pb + 8, pc, 64, 64, 64) == ALIGN      # misaligned B
+    assert plan.status_run(pa, pb, pc + 4, 64, 64, 64) == ALIGN      # misaligned C
+    assert plan.status_run(0, pb, pc, 64, 64, 64) == INVALID         # null A
+    assert plan.status_run(pa, pb, 0, 64, 64, 64) == INVALID         # null C
+    assert plan.status_run(pa, pb, pc, -1, 64, 64) == INVALID
+    assert plan.status_run(pa, pb, pc, 64, 64, 1 << 31) == INVALID
+    assert plan.status_run(pa, pb, pc, 64, 64, 64, acc=2) == INVALID
+    assert plan.status_run(pa, pb, pa, 64, 64, 64) == INVALID        # C aliases A
+    torch.cuda.synchronize()
+    assert bool((c == 3.0).all())
+
+
+def test_writes_stay_inside_C(plan):
+    """C sits inside a larger buffer of sentinels; a ragged shape must leave
+    every byte before and after it untouched."""
+    M, N, K = 203, 264, 200
+    a, b = wl.draw(M, N, K, seed=31)
+    guard = 4096
+    buf = torch.full((guard + M * N + guard,), 1234.0, dtype=torch.float16, device="cuda")
+    c = buf[guard:guard + M * N].view(M, N)
+    plan.run(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), c)
+    plan.check_error()
+    host = buf.cpu()
+    assert bool((host[:guard] == 1234.0).all()) and bool((host[guard + M * N:] == 1234.0).all())
+    assert_close(c.cpu().numpy(), oracle.gemm_f64(a, b), "f32", "guarded")
+
+
+def test_repeated_launches_stay_clean(plan):
+    """Many back-to-back launches into a NaN-filled C: no NaN may ever appear
+    (the symptom of a barrier placed inside a live TMA destination, tilus
+    "A Minimal Hopper Matmul", Epilogue note)."""
+    M, N, K = 1024, 2048, 1024
+    a, b = wl.draw(M, N, K, seed=32)
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    first = None
+    for i in range(40):
+        c = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        plan.run(ta, tb, c, acc="f32" if i % 2 == 0 else "f16")
+        if i % 2 == 0:
+            if first is None:
+                first = c.clone()
+            else:
+                assert torch.equal(c, first), f"launch {i} differs from launch 0"
+        assert not bool(torch.isnan(c).any()), f"NaN in launch {i}"
+    plan.check_error()
+
+
+def test_side_stream(plan):
+    M, N, K = 384, 512, 256
+    a, b = wl.draw(M, N, K, seed=33)
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    s = torch.cuda.Stream()
+    c = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    with torch.cuda.stream(s):
+        plan.run(ta, tb, c)
+    s.synchronize()
+    plan.check_error()
+    assert_close(c.cpu().numpy(), oracle.gemm_f64(a, b), "f32", "side stream")
+
+
+@pytest.mark.parametrize("acc", ["f32", "f16"])
+def test_host_entry_point_matches_device_entry_point(plan, acc):
+    M, N, K = 700, 1032, 520
+    a, b = wl.draw(M, N, K, seed=34)
+    dev = run_gpu(plan, a, b, acc)
+    ha = torch.from_numpy(a).pin_memory()
+    hb = torch.from_numpy(b).pin_memory()
+    hc = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    plan.run_host(ha, hb, hc, acc=acc)
+    assert np.array_equal(hc.numpy().view(np.uint16), dev.view(np.uint16))
+    # pageable numpy buffers work too
+    out = np.empty((M, N), np.float16)
+    plan.run_host(a, b, out, acc=acc)
+    assert np.array_equal(out.view(np.uint16), dev.view(np.uint16))
+
+
+def test_gemm_convenience_wrapper(plan):
+    a, b = wl.draw(256, 264, 128, seed=35)
+    c = g.gemm(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
+    torch.cuda.synchronize()
+    assert_close(c.cpu().numpy(), oracle.gemm_f64(a, b), "f32", "gemm()")
+
+
+def test_variant_choice_and_launch_count(plan):
+    name, grid = plan.pick_variant(8192, 8192, 8192)
+    assert name in g.variant_names() and grid >= 1
+    n0 = plan.launch_count
+    run_gpu(plan, *wl.draw(128, 128, 64, seed=36))
+    assert plan.launch_count == n0 + 1
