@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "gemm.h"
@@ -393,3 +394,138 @@ gemm_status_t gemm_run_host(gemm_plan_t p, const void* A, const void* B, void* C
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot call cudaMalloc: code running under an allocator that
+// owns every byte of device memory (a framework's caching allocator, or a
+// fixed arena carved out at start-up, where a stray cudaMalloc can fail or
+// fragment the pool), and latency-bound loops where cudaMalloc's implicit
+// device synchronisation would stall other streams.  gemm_plan_create
+// allocates the kernel's watchdog record with cudaMalloc, so such callers
+// cannot make a plan.  gemm_run_noalloc runs the same kernel with that
+// scratch -- the 16-byte watchdog record, the only global memory the kernel
+// touches beyond A, B and C -- in the file-scope array below instead.
+//
+// The array is a static device variable: every GPU that loads this library
+// holds its 256 bytes until the process exits.  In host code its name is only
+// a host-side stand-in, never a device address, so each device's address is
+// looked up once with cudaGetSymbolAddress (with that device current) and
+// that address is what the kernel receives.
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint32_t)];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+// Scratch the single-CTA kernel needs for one call, whatever the shape.
+constexpr size_t kNoAllocRecordBytes = 4 * sizeof(uint32_t);
+
+struct NoAllocDevice {
+  std::once_flag once;
+  gemm_status_t status = GEMM_ERR_CUDA;
+  int num_sms = 0;
+  uint32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::once_flag g_noalloc_encode_once;
+EncodeTiledFn g_noalloc_encode = nullptr;
+
+// One-time set-up for the current device `dev`.
+gemm_status_t noalloc_setup(int dev, NoAllocDevice& d) {
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
+  std::call_once(g_noalloc_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_noalloc_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  if (!g_noalloc_encode) return GEMM_ERR_CUDA;
+  if (set_smem_attr<SingleF32>() != cudaSuccess || set_smem_attr<SingleF16>() != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return GEMM_ERR_CUDA;
+  d.scratch = static_cast<uint32_t*>(ptr);
+  d.num_sms = sms;
+  return GEMM_OK;
+}
+
+bool noalloc_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows, uint32_t box_cols) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_noalloc_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M,
+                                          int64_t N, int64_t K, gemm_acc_t acc, void* stream) {
+  gemm_status_t s = check_shape(M, N, K, acc);
+  if (s != GEMM_OK) return s;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(C) & 15) ||
+      (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))))
+    return GEMM_ERR_ALIGNMENT;
+  const size_t bytesC = static_cast<size_t>(M) * N * 2;
+  if (K > 0 && (overlaps(C, bytesC, A, static_cast<size_t>(M) * K * 2) ||
+                overlaps(C, bytesC, B, static_cast<size_t>(N) * K * 2)))
+    return GEMM_ERR_INVALID_ARG;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return GEMM_ERR_CUDA;
+  if (dev >= kNoAllocMaxDevices) return GEMM_ERR_INVALID_ARG;
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  std::call_once(d.once, [&] { d.status = noalloc_setup(dev, d); });
+  if (d.status != GEMM_OK) return d.status;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) {  // the empty sum: zeros, no scratch involved
+    const int64_t n16 = M * N * 2 / 16;
+    const int64_t blocks = (n16 + 255) / 256;
+    gb300::gemm_zero_fill<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(
+        static_cast<uint4*>(C), n16);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+  // The scratch this call needs must fit the array.
+  if (kNoAllocRecordBytes > kNoAllocScratchBytes) return GEMM_ERR_INVALID_ARG;
+
+  const VariantInfo& vi = kVariants[0];
+  CUtensorMap ma, mb, mc;
+  if (!noalloc_map(&ma, A, M, K, vi.tile_m, 64) || !noalloc_map(&mb, B, N, K, vi.tile_n, 64) ||
+      !noalloc_map(&mc, C, M, N, 32, 64))
+    return GEMM_ERR_CUDA;
+  GemmArgs args;
+  args.M = static_cast<int32_t>(M);
+  args.N = static_cast<int32_t>(N);
+  args.K = static_cast<int32_t>(K);
+  args.tiles_m = static_cast<int32_t>((M + vi.tile_m - 1) / vi.tile_m);
+  args.tiles_n = static_cast<int32_t>((N + vi.tile_n - 1) / vi.tile_n);
+  args.num_kb = static_cast<int32_t>((K + 63) / 64);
+  args.num_tiles = args.tiles_m * args.tiles_n;
+  args.group_m = kGroupM;
+  args.err = d.scratch;
+  args.timeout_ns = kDefaultTimeoutNs;
+  args.skip_kb = -1;
+  const int grid = args.num_tiles < d.num_sms ? args.num_tiles : d.num_sms;
+  // The watchdog record must start at zero; the array keeps the last call's
+  // contents, so clear it on the caller's stream before the launch.
+  if (cudaMemsetAsync(d.scratch, 0, kNoAllocRecordBytes, st) != cudaSuccess) return GEMM_ERR_CUDA;
+  cudaError_t e = acc == GEMM_ACC_F32 ? launch_single<SingleF32>(ma, mb, mc, args, grid, st)
+                                      : launch_single<SingleF16>(ma, mb, mc, args, grid, st);
+  return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}

@@ -135,6 +135,33 @@ GEMM_API int32_t gemm_plan_pick_variant(gemm_plan_t plan, int64_t M, int64_t N, 
  * gemm_run_host; the K == 0 zero-fill counts as one). */
 GEMM_API uint64_t gemm_plan_launch_count(gemm_plan_t plan);
 
+/* C = A x B^T exactly as gemm_run computes it, for callers that cannot
+ * allocate device memory: no plan, and no cudaMalloc, cudaFree or allocating
+ * library call anywhere in the call.  Who needs it: code running under an
+ * allocator that owns all device memory (a framework's caching allocator or a
+ * fixed arena, where a stray cudaMalloc can fail or fragment the pool), and
+ * latency-bound loops that cannot afford cudaMalloc's implicit device
+ * synchronisation.  The tutorial pages have no counterpart: this entry point
+ * exists for those callers only.
+ *
+ * Arguments, layouts, shape and alignment rules, and the K == 0 / empty
+ * cases are those of gemm_run; the device is the caller's current device.
+ * The kernel's only scratch (its 16-byte watchdog record) lives in a static
+ * 256-byte device array inside the library, which every GPU that loads the
+ * library holds until the process exits; a call whose scratch would not fit
+ * is rejected with GEMM_ERR_INVALID_ARG (no current shape needs more than
+ * 16 bytes).  The first call on each device does a one-time set-up (device
+ * checks, kernel attributes, and the device address of the array via
+ * cudaGetSymbolAddress), so make that first call before any stream capture.
+ * Each call clears the record on `stream` before its launch.  All calls share
+ * the one array: calls that overlap on the GPU race on it.  A watchdog
+ * timeout cannot be reported by this asynchronous call: the kernel returns
+ * early with C incomplete, and the next call clears the record; callers who
+ * need the timeout report use gemm_run with a plan. */
+GEMM_API gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
+                                        int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
+                                        void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 GEMM_API const char* gemm_status_string(gemm_status_t s);
 
