@@ -17,8 +17,8 @@
 
 namespace {
 
-using gb300::CfgSingle;
 using gb300::GemmArgs;
+using gb300::GemmCfg;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -27,17 +27,25 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 // ------------------------------------------------------------ the variants --
 // Compile-time tile configurations; the host picks one per call.
-using SingleF32 = CfgSingle<256, 4, false>;
-using SingleF16 = CfgSingle<256, 4, true>;
+using PairF32 = GemmCfg<2, 6, false>;    // CTA pair, 256 x 256 tile, 6 stages
+using PairF16 = GemmCfg<2, 6, true>;
+using SingleF32 = GemmCfg<1, 4, false>;  // one CTA, 128 x 256 tile, 4 stages
+using SingleF16 = GemmCfg<1, 4, true>;
 
 struct VariantInfo {
   const char* name;
-  int tile_m, tile_n;  // output tile owned by one CTA
+  int ctas;            // CTAs per tile (cluster size)
+  int tile_m, tile_n;  // output tile owned by one CTA or CTA pair
+  int box_a_rows;      // rows of A each CTA loads per stage
+  int box_b_rows;      // rows of B each CTA loads per stage
 };
 
-constexpr int kNumVariants = 1;
+constexpr int kVariantPair = 0;
+constexpr int kVariantSingle = 1;
+constexpr int kNumVariants = 2;
 constexpr VariantInfo kVariants[kNumVariants] = {
-    {"tc_single_128x256_s4", 128, 256},
+    {"tc_pair_256x256_s6", 2, 256, 256, 128, 128},
+    {"tc_single_128x256_s4", 1, 128, 256, 128, 256},
 };
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s for any single wait
@@ -57,6 +65,7 @@ struct MapEntry {
 struct gemm_plan_s {
   int device = 0;
   int num_sms = 0;
+  int max_pairs = 0;  // CTA pairs of the pair kernel that fit on the device at once
   EncodeTiledFn encode = nullptr;
   uint32_t* d_err = nullptr;  // 4-word watchdog record
   uint32_t last_err[4] = {0, 0, 0, 0};
@@ -140,26 +149,69 @@ gemm_status_t check_shape(int64_t M, int64_t N, int64_t K, gemm_acc_t acc) {
   return GEMM_OK;
 }
 
+int64_t tiles_of(const VariantInfo& vi, int64_t M, int64_t N) {
+  return ((M + vi.tile_m - 1) / vi.tile_m) * ((N + vi.tile_n - 1) / vi.tile_n);
+}
+
+// Grid in CTAs: one CTA (or pair) per tile up to what fits on the device.
+int grid_for(const VariantInfo& vi, int64_t tiles, int num_sms, int max_pairs) {
+  if (vi.ctas == 2) {
+    const int64_t pairs = tiles < max_pairs ? tiles : max_pairs;
+    return static_cast<int>(2 * pairs);
+  }
+  return static_cast<int>(tiles < num_sms ? tiles : num_sms);
+}
+
 int pick_variant(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, int* grid) {
-  int v = p->forced_variant >= 0 ? p->forced_variant : 0;
+  int v = p->forced_variant >= 0 ? p->forced_variant : kVariantPair;
+  if (kVariants[v].ctas == 2 && p->max_pairs < 1) v = kVariantSingle;
   const VariantInfo& vi = kVariants[v];
-  const int64_t tiles = ((M + vi.tile_m - 1) / vi.tile_m) * ((N + vi.tile_n - 1) / vi.tile_n);
   (void)K;
-  if (grid) *grid = static_cast<int>(tiles < p->num_sms ? tiles : p->num_sms);
+  if (grid) *grid = grid_for(vi, tiles_of(vi, M, N), p->num_sms, p->max_pairs);
   return v;
 }
 
 template <class Cfg>
-cudaError_t launch_single(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                          const GemmArgs& args, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const GemmArgs& args, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, gb300::gemm_tc_single<Cfg>, a, b, c, args);
+  if (Cfg::kCtas == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, gb300::gemm_tc_kernel<Cfg>, a, b, c, args);
+}
+
+template <class Cfg>
+int max_active_pairs() {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gb300::gemm_tc_kernel<Cfg>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, int64_t M,
@@ -176,7 +228,7 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   const int v = pick_variant(p, M, N, K, &grid);
   const VariantInfo& vi = kVariants[v];
   CUtensorMap ma, mb, mc;
-  if (!get_map(p, &ma, A, M, K, vi.tile_m, 64) || !get_map(p, &mb, B, N, K, vi.tile_n, 64) ||
+  if (!get_map(p, &ma, A, M, K, vi.box_a_rows, 64) || !get_map(p, &mb, B, N, K, vi.box_b_rows, 64) ||
       !get_map(p, &mc, C, M, N, 32, 64))
     return GEMM_ERR_CUDA;
 
@@ -193,15 +245,20 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   args.timeout_ns = p->timeout_ns;
   args.skip_kb = p->skip_kb;
 
-  cudaError_t e = acc == GEMM_ACC_F32 ? launch_single<SingleF32>(ma, mb, mc, args, grid, stream)
-                                      : launch_single<SingleF16>(ma, mb, mc, args, grid, stream);
+  cudaError_t e;
+  if (vi.ctas == 2)
+    e = acc == GEMM_ACC_F32 ? launch_gemm<PairF32>(ma, mb, mc, args, grid, stream)
+                            : launch_gemm<PairF16>(ma, mb, mc, args, grid, stream);
+  else
+    e = acc == GEMM_ACC_F32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, stream)
+                            : launch_gemm<SingleF16>(ma, mb, mc, args, grid, stream);
   ++p->launches;
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 template <class Cfg>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gb300::gemm_tc_single<Cfg>,
+  return cudaFuncSetAttribute(gb300::gemm_tc_kernel<Cfg>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
 }
 
@@ -272,9 +329,14 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     return GEMM_ERR_CUDA;
   }
   p->encode = reinterpret_cast<EncodeTiledFn>(fn);
-  if (set_smem_attr<SingleF32>() != cudaSuccess || set_smem_attr<SingleF16>() != cudaSuccess) {
+  if (set_smem_attr<SingleF32>() != cudaSuccess || set_smem_attr<SingleF16>() != cudaSuccess ||
+      set_smem_attr<PairF32>() != cudaSuccess || set_smem_attr<PairF16>() != cudaSuccess) {
     delete p;
     return GEMM_ERR_CUDA;
+  }
+  {
+    const int a = max_active_pairs<PairF32>(), b = max_active_pairs<PairF16>();
+    p->max_pairs = a < b ? a : b;
   }
   if (cudaMalloc(&p->d_err, 4 * sizeof(uint32_t)) != cudaSuccess) {
     delete p;
@@ -504,9 +566,9 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   // The scratch this call needs must fit the array.
   if (kNoAllocRecordBytes > kNoAllocScratchBytes) return GEMM_ERR_INVALID_ARG;
 
-  const VariantInfo& vi = kVariants[0];
+  const VariantInfo& vi = kVariants[kVariantSingle];
   CUtensorMap ma, mb, mc;
-  if (!noalloc_map(&ma, A, M, K, vi.tile_m, 64) || !noalloc_map(&mb, B, N, K, vi.tile_n, 64) ||
+  if (!noalloc_map(&ma, A, M, K, vi.box_a_rows, 64) || !noalloc_map(&mb, B, N, K, vi.box_b_rows, 64) ||
       !noalloc_map(&mc, C, M, N, 32, 64))
     return GEMM_ERR_CUDA;
   GemmArgs args;
@@ -525,7 +587,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   // The watchdog record must start at zero; the array keeps the last call's
   // contents, so clear it on the caller's stream before the launch.
   if (cudaMemsetAsync(d.scratch, 0, kNoAllocRecordBytes, st) != cudaSuccess) return GEMM_ERR_CUDA;
-  cudaError_t e = acc == GEMM_ACC_F32 ? launch_single<SingleF32>(ma, mb, mc, args, grid, st)
-                                      : launch_single<SingleF16>(ma, mb, mc, args, grid, st);
+  cudaError_t e = acc == GEMM_ACC_F32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, st)
+                                      : launch_gemm<SingleF16>(ma, mb, mc, args, grid, st);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -3,25 +3,33 @@
 //   C[M,N] = A[M,K] x B[N,K]^T, fp16 in, fp32 or fp16 accumulate, fp16 out
 //   (tilus "A Minimal Hopper Matmul", section "Block Tiling").
 //
-// One CTA per SM loops over output tiles (static stride over a grouped
-// raster).  Inside the CTA the work is split by warp, as in the producer /
-// consumer split of tilus "Warp Specialization", redesigned for tcgen05:
+// One template, two forms:
+//   kCtas = 1  one CTA per SM owns a 128 x 256 output tile;
+//   kCtas = 2  a cluster of two CTAs on neighbouring SMs owns a 256 x 256
+//              tile: each CTA loads its 128 rows of A and half (128 rows) of
+//              B, and one thread of the leader CTA issues
+//              tcgen05.mma.cta_group::2 (M = 256) over both CTAs' shared
+//              memory, so every SM stages a third less operand data per FLOP.
 //
-//   warp 0, lane 0   TMA producer: fills a kStages-deep ring of A/B k-blocks,
-//                    one "full" mbarrier (transaction bytes) per stage.
-//   warp 1           allocates tensor memory; lane 0 issues every tcgen05.mma
-//                    of the CTA and releases each stage with tcgen05.commit
-//                    onto its "empty" mbarrier.
+// CTAs (or pairs) are persistent and walk the tiles with a static stride over
+// a grouped raster.  Inside a CTA the work is split by warp, after the
+// producer / consumer split of tilus "Warp Specialization", redesigned for
+// tcgen05:
+//
+//   warp 0, lane 0   TMA producer: fills a kStages-deep ring of A/B k-blocks.
+//   warp 1           allocates tensor memory (TMEM); lane 0 of the leader CTA
+//                    issues every tcgen05.mma and releases each stage with
+//                    tcgen05.commit onto its "empty" mbarrier(s).
 //   warps 2..5       epilogue: tcgen05.ld the accumulator, round to fp16,
 //                    stage through swizzled shared memory, TMA-store.
 //
-// The accumulator lives in tensor memory, double-buffered (2 x BN columns),
-// so the epilogue of tile i overlaps the main loop of tile i+1; two more
-// barrier pairs (tmem_full / tmem_empty) hand the buffers back and forth.
+// The accumulator is double-buffered in TMEM (2 x 256 columns), so the
+// epilogue of one tile overlaps the main loop of the next; tmem_full /
+// tmem_empty barriers hand the buffers back and forth.
 //
 // Every wait is bounded: a wait that outlives the timeout records the site in
-// a device watchdog word, raises a CTA-wide abort flag, and every role then
-// leaves its loop; the CTA waits (again bounded) for its own loads and MMAs,
+// a device watchdog word and raises the CTA's abort flag; every role then
+// leaves its loop, the CTA waits (again bounded) for its own loads and MMAs,
 // frees tensor memory and returns.
 #pragma once
 #include <cuda_fp16.h>
@@ -53,14 +61,21 @@ struct GemmArgs {
   int32_t skip_kb;      // fault injection, -1 = off
 };
 
-// Tile configuration of the single-CTA kernel.
-template <int kBN_, int kStages_, bool kAccF16_>
-struct CfgSingle {
-  static constexpr int kBM = 128, kBN = kBN_, kBK = 64, kStages = kStages_;
+// Tile configuration.  kCtas CTAs cooperate on one tile of kTileM x kBN.
+template <int kCtas_, int kStages_, bool kAccF16_>
+struct GemmCfg {
+  static constexpr int kCtas = kCtas_;
+  static constexpr int kBM = 128;                 // rows of C per CTA
+  static constexpr int kBN = 256;                 // columns of C per tile
+  static constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle row)
+  static constexpr int kTileM = kBM * kCtas;      // rows of C per tile
+  static constexpr int kBRows = kBN / kCtas;      // rows of B each CTA loads
+  static constexpr int kStages = kStages_;
   static constexpr bool kAccF16 = kAccF16_;
   static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = kBN * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBBytes = kBRows * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;  // landed in each CTA per stage
+  static constexpr int kTxBytes = kStageBytes * kCtas;   // counted on the leader's barrier
   static constexpr int kEpiWarps = 4;
   static constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 fp16, 128B swizzle
   static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
@@ -74,10 +89,10 @@ struct CfgSingle {
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
   static constexpr int kTmemCols = 2 * kBN;
   static constexpr int kThreads = 192;
-  static constexpr uint32_t kIdesc = ptx::idesc_f16(kBM, kBN, !kAccF16);
+  static constexpr uint32_t kIdesc = ptx::idesc_f16(kTileM, kBN, !kAccF16);
 
-  static_assert(kBN % 64 == 0 && kBN >= 64 && kBN <= 256, "BN must be 64..256 in steps of 64");
-  static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM columns: power of 2");
+  static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair");
+  static_assert(kTmemCols == 512, "two 256-column accumulators fill TMEM");
   static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory per CTA");
   static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1024 B alignment");
   // Barriers sit after every TMA destination, never inside one (tilus "A
@@ -94,11 +109,14 @@ struct Watch {
 
 // Slow path of a bounded mbarrier wait.  Returns false when the wait gave up,
 // either because the CTA is aborting (and honor_abort) or after timeout_ns.
+template <bool kClusterScope>
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Watch w, uint32_t site,
                                        int32_t tile, bool honor_abort) {
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const bool done = kClusterScope ? ptx::mbar_try_wait_cluster(bar, parity)
+                                    : ptx::mbar_try_wait(bar, parity);
+    if (done) return true;
     if (honor_abort && *w.abort) return false;
     if (ptx::globaltimer_ns() - t0 > w.timeout_ns) {
       if (atomicCAS(w.err, 0u, kStatusTimeout) == 0u) {
@@ -112,15 +130,18 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Watch w, u
   }
 }
 
+template <bool kClusterScope>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Watch& w,
                                          uint32_t site, int32_t tile, bool honor_abort = true) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, w, site, tile, honor_abort);
+  const bool done =
+      kClusterScope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+  if (done) return true;
+  return wait_slow<kClusterScope>(bar, parity, w, site, tile, honor_abort);
 }
 
 // Grouped raster: tiles are walked down a group of `group` tile-rows before
-// moving one tile-column right, so CTAs running at the same time share A rows
-// and B rows in L2.  A bijection of [0, tiles_m*tiles_n).
+// moving one tile-column right, so tiles in flight at the same time share A
+// rows and B rows in L2.  A bijection of [0, tiles_m*tiles_n).
 __device__ __forceinline__ void raster(int32_t t, int32_t tiles_m, int32_t tiles_n, int32_t group,
                                        int32_t& mb, int32_t& nb) {
   const int32_t per = group * tiles_n;
@@ -139,15 +160,20 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
-    gemm_tc_single(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   constexpr int S = Cfg::kStages;
+  constexpr bool kPair = Cfg::kCtas == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = ptx::smem_addr(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Position of this CTA in its pair and of the pair in the grid.
+  const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
+  const int32_t unit = kPair ? static_cast<int32_t>(ptx::cluster_id_x()) : static_cast<int32_t>(blockIdx.x);
+  const int32_t units = kPair ? static_cast<int32_t>(ptx::num_clusters_x()) : static_cast<int32_t>(gridDim.x);
 
   const uint32_t bar0 = sb + Cfg::kOffBar;
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
@@ -170,18 +196,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(bar_tfull(b), 1);
-      ptx::mbar_init(bar_tempty(b), Cfg::kEpiWarps);
+      ptx::mbar_init(bar_tempty(b), Cfg::kEpiWarps * Cfg::kCtas);
     }
     ptx::mbar_init(bar_mma_done, 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc<1>(sb + Cfg::kOffSlot, Cfg::kTmemCols);
-    ptx::tmem_relinquish<1>();
+    ptx::tmem_alloc<Cfg::kCtas>(sb + Cfg::kOffSlot, Cfg::kTmemCols);
+    ptx::tmem_relinquish<Cfg::kCtas>();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair)
+    ptx::cluster_sync();  // both CTAs' barriers exist before either uses the other's
+  else
+    __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffSlot);
 
@@ -192,20 +221,30 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       uint32_t phase = 0;
       int64_t fills = 0;
       bool ok = true;
-      for (int32_t tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+      for (int32_t tile = unit; ok && tile < args.num_tiles; tile += units) {
         int32_t mb, nb;
         raster(tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
+        const int32_t a_row = mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM;
+        const int32_t b_row = nb * Cfg::kBN + static_cast<int32_t>(rank) * Cfg::kBRows;
         for (int32_t kb = 0; kb < args.num_kb; ++kb) {
-          if (!wait_bar(bar_empty(stage), phase ^ 1u, w, kSiteEmpty, tile)) {
+          if (!wait_bar<kPair>(bar_empty(stage), phase ^ 1u, w, kSiteEmpty, tile)) {
             ok = false;
             break;
           }
-          const bool skip = args.skip_kb == kb && tile == static_cast<int32_t>(blockIdx.x) &&
-                            blockIdx.x == 0;
+          const bool skip = args.skip_kb == kb && tile == unit && unit == 0 && rank == 0;
           if (!skip) {
-            ptx::mbar_arrive_expect_tx(bar_full(stage), Cfg::kStageBytes);
-            ptx::tma_load_2d(sA(stage), &tmA, bar_full(stage), kb * Cfg::kBK, mb * Cfg::kBM);
-            ptx::tma_load_2d(sB(stage), &tmB, bar_full(stage), kb * Cfg::kBK, nb * Cfg::kBN);
+            if constexpr (kPair) {
+              // Both CTAs' bytes are counted on the leader's full barrier; the
+              // leader declares them all.
+              const uint32_t full_leader = ptx::mapa(bar_full(stage), 0);
+              if (rank == 0) ptx::mbar_arrive_expect_tx(bar_full(stage), Cfg::kTxBytes);
+              ptx::tma_load_2d_pair(sA(stage), &tmA, full_leader, kb * Cfg::kBK, a_row);
+              ptx::tma_load_2d_pair(sB(stage), &tmB, full_leader, kb * Cfg::kBK, b_row);
+            } else {
+              ptx::mbar_arrive_expect_tx(bar_full(stage), Cfg::kTxBytes);
+              ptx::tma_load_2d(sA(stage), &tmA, bar_full(stage), kb * Cfg::kBK, a_row);
+              ptx::tma_load_2d(sB(stage), &tmB, bar_full(stage), kb * Cfg::kBK, b_row);
+            }
           }
           ++fills;
           if (++stage == S) {
@@ -217,35 +256,36 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // Drain: the last min(S, fills) fills may still be in use.  Normally
       // wait until the MMA issuer has released each of them, so no tcgen05
       // arrival is still headed for the ring when the CTA exits (tilus "Warp
-      // Specialization", "Draining the Pipeline").  When aborting, wait
-      // instead (bounded, ignoring the abort flag) for those loads to land.
+      // Specialization", "Draining the Pipeline").  When aborting, the CTA
+      // holding the full barriers waits instead (bounded, ignoring the abort
+      // flag) for those loads to land.
       const int64_t n = fills < S ? fills : S;
       for (int64_t f = fills - n; f < fills; ++f) {
         const int s = static_cast<int>(f % S);
         const uint32_t par = static_cast<uint32_t>((f / S) & 1);
-        if (ok)
-          ok = wait_bar(bar_empty(s), par, w, kSiteDrain, -1);
-        if (!ok) wait_bar(bar_full(s), par, w, kSiteDrain, -1, /*honor_abort=*/false);
+        if (ok) ok = wait_bar<kPair>(bar_empty(s), par, w, kSiteDrain, -1);
+        if (!ok && rank == 0)
+          wait_bar<kPair>(bar_full(s), par, w, kSiteDrain, -1, /*honor_abort=*/false);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ------------------------------------------------------- MMA issuer --
       int stage = 0;
       uint32_t phase = 0;
       int32_t acc_iter = 0;
       bool ok = true;
-      for (int32_t tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+      for (int32_t tile = unit; ok && tile < args.num_tiles; tile += units) {
         const int buf = acc_iter & 1;
         const uint32_t use_par = static_cast<uint32_t>((acc_iter >> 1) & 1);
-        if (!wait_bar(bar_tempty(buf), use_par ^ 1u, w, kSiteTmemEmpty, tile)) {
+        if (!wait_bar<kPair>(bar_tempty(buf), use_par ^ 1u, w, kSiteTmemEmpty, tile)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kBN);
         for (int32_t kb = 0; kb < args.num_kb; ++kb) {
-          if (!wait_bar(bar_full(stage), phase, w, kSiteFull, tile)) {
+          if (!wait_bar<kPair>(bar_full(stage), phase, w, kSiteFull, tile)) {
             ok = false;
             break;
           }
@@ -255,43 +295,55 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < Cfg::kBK / 16; ++k) {
             // +32 bytes along K per 16-element step, inside the swizzled row
-            ptx::mma_f16<1>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
-                            (kb | k) != 0 ? 1u : 0u);
+            ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+                                     (kb | k) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(bar_empty(stage));
+          if constexpr (kPair)
+            ptx::mma_commit_pair(bar_empty(stage), 0x3);
+          else
+            ptx::mma_commit(bar_empty(stage));
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(bar_tfull(buf));
+        if constexpr (kPair)
+          ptx::mma_commit_pair(bar_tfull(buf), 0x3);
+        else
+          ptx::mma_commit(bar_tfull(buf));
         ++acc_iter;
       }
       // Every MMA this thread issued has finished before tensor memory is
       // freed (bounded, whatever the abort state).
-      ptx::mma_commit(bar_mma_done);
-      wait_bar(bar_mma_done, 0u, w, kSiteMmaDone, -1, /*honor_abort=*/false);
+      if constexpr (kPair)
+        ptx::mma_commit_pair(bar_mma_done, 0x1);
+      else
+        ptx::mma_commit(bar_mma_done);
+      wait_bar<kPair>(bar_mma_done, 0u, w, kSiteMmaDone, -1, /*honor_abort=*/false);
     }
   } else {
     // ------------------------------------------------------------ epilogue --
     const int q = warp & 3;  // this warp may touch TMEM lanes 32q .. 32q+31 only
     const uint32_t stage_base = sb + Cfg::kOffEpi + static_cast<uint32_t>(q * 2 * Cfg::kEpiBufBytes);
+    // tmem_empty lives in the leader CTA: every epilogue warp of the pair
+    // arrives there.
+    const uint32_t tempty_bar0 = kPair ? ptx::mapa(bar_tempty(0), 0) : bar_tempty(0);
     uint32_t stores = 0;
     int32_t acc_iter = 0;
-    for (int32_t tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
+    for (int32_t tile = unit; tile < args.num_tiles; tile += units) {
       int32_t mb, nb;
       raster(tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
       const int buf = acc_iter & 1;
       const uint32_t use_par = static_cast<uint32_t>((acc_iter >> 1) & 1);
       int ok = 1;
-      if (lane == 0) ok = wait_bar(bar_tfull(buf), use_par, w, kSiteTmemFull, tile) ? 1 : 0;
+      if (lane == 0) ok = wait_bar<kPair>(bar_tfull(buf), use_par, w, kSiteTmemFull, tile) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * Cfg::kBN);
-      const int32_t row0 = mb * Cfg::kBM + q * 32;
+      const int32_t row0 = mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM + q * 32;
 #pragma unroll 1
       for (int c = 0; c < Cfg::kBN / 64; ++c) {
         uint32_t packed[32];
@@ -313,7 +365,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           // The whole accumulator buffer is in registers: hand it back.
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar_tempty(buf));
+          if (lane == 0) {
+            if constexpr (kPair)
+              ptx::mbar_arrive_cluster(tempty_bar0 + 8u * buf);
+            else
+              ptx::mbar_arrive(tempty_bar0 + 8u * buf);
+          }
         }
         const uint32_t sbuf = stage_base + (stores & 1u) * Cfg::kEpiBufBytes;
         if (stores >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();
@@ -344,10 +401,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair)
+    ptx::cluster_sync();  // no CTA leaves while its peer may still touch its memory
+  else
+    __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc<1>(tmem_base, Cfg::kTmemCols);
+    ptx::tmem_dealloc<Cfg::kCtas>(tmem_base, Cfg::kTmemCols);
   }
 }
 

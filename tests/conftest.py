@@ -78,13 +78,33 @@ def assert_close(got, ref, acc, what=""):
     return st
 
 
+# Kernel variants of the library, in its table order (checked against the
+# library by test_abi_host.py::test_variant_table).
+VARIANTS = ["tc_pair_256x256_s6", "tc_single_128x256_s4"]
+
+
 @pytest.fixture(scope="session")
 def plan():
+    """A plan with automatic variant choice."""
     import dense_fp16_gemm_04_gb300 as g
     g.build()
     p = g.Plan(0)
     yield p
     p.close()
+
+
+@pytest.fixture(scope="session")
+def plans():
+    """One plan per kernel variant, each forced to that variant."""
+    import dense_fp16_gemm_04_gb300 as g
+    g.build()
+    ps = {}
+    for name in VARIANTS:
+        ps[name] = g.Plan(0)
+        ps[name].set_variant(name)
+    yield ps
+    for p in ps.values():
+        p.close()
 
 
 def to_dev(x):

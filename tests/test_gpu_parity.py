@@ -8,17 +8,23 @@ import torch
 
 import gemm_workloads as wl
 import oracle
-from conftest import TOL, assert_close, error_stats, read_golden, run_gpu, to_dev
+from conftest import TOL, VARIANTS, assert_close, error_stats, read_golden, run_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("acc", ["f32", "f16"])
-def test_512_full(plan, acc):
+def test_512_full(plans, variant, acc):
     w = wl.WORKLOADS["gemm_512"]
     a, b = wl.inputs_for(w)
     ref = oracle.gemm_f64(a, b)
-    assert_close(run_gpu(plan, a, b, acc), ref, acc, f"512^3 {acc}")
+    assert_close(run_gpu(plans[variant], a, b, acc), ref, acc, f"512^3 {acc} {variant}")
+
+
+def test_auto_variant_512(plan):
+    a, b = wl.inputs_for(wl.WORKLOADS["gemm_512"])
+    assert_close(run_gpu(plan, a, b), oracle.gemm_f64(a, b), "f32", "auto")
 
 
 # Shapes spanning several tiles with ragged M, N and K tails, short K (fewer
@@ -30,12 +36,14 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("acc", ["f32", "f16"])
-def test_shapes_full(plan, shape, acc):
+def test_shapes_full(plans, variant, shape, acc):
     M, N, K = shape
     a, b = wl.draw(M, N, K, seed=M * 7 + N * 3 + K)
-    assert_close(run_gpu(plan, a, b, acc), oracle.gemm_f64(a, b), acc, f"{shape} {acc}")
+    assert_close(run_gpu(plans[variant], a, b, acc), oracle.gemm_f64(a, b), acc,
+                 f"{shape} {acc} {variant}")
 
 
 def test_bt_convention_fixture(plan):
@@ -54,42 +62,47 @@ def test_bt_convention_fixture(plan):
 
 @pytest.mark.parametrize("acc,K", [("f32", 8), ("f32", 4104), ("f32", 8192),
                                    ("f16", 64), ("f16", 2048)])
-def test_all_ones_exact(plan, acc, K):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_all_ones_exact(plans, variant, acc, K):
     a, b = wl.ones(300, 264, K)
-    c = run_gpu(plan, a, b, acc)
+    c = run_gpu(plans[variant], a, b, acc)
     assert np.array_equal(c.astype(np.float64), np.full((300, 264), float(K)))
 
 
 @pytest.mark.parametrize("acc", ["f32", "f16"])
-def test_identity_left_gives_B_transposed(plan, acc):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_identity_left_gives_B_transposed(plans, variant, acc):
     K, N = 264, 136
     _, b = wl.draw(K, N, K, seed=21)
-    c = run_gpu(plan, wl.identity(K), b, acc)
+    c = run_gpu(plans[variant], wl.identity(K), b, acc)
     assert np.array_equal(c.view(np.uint16), np.ascontiguousarray(b.T).view(np.uint16))
 
 
 @pytest.mark.parametrize("acc", ["f32", "f16"])
-def test_identity_right_gives_A(plan, acc):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_identity_right_gives_A(plans, variant, acc):
     M, K = 200, 264
     a, _ = wl.draw(M, K, K, seed=22)
-    c = run_gpu(plan, a, wl.identity(K), acc)
+    c = run_gpu(plans[variant], a, wl.identity(K), acc)
     assert np.array_equal(c.view(np.uint16), a.view(np.uint16))
 
 
 @pytest.mark.parametrize("acc", ["f32", "f16"])
-def test_permutation_selects_columns(plan, acc):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_permutation_selects_columns(plans, variant, acc):
     M, N, K = 160, 256, 512
     a, _ = wl.draw(M, N, K, seed=23)
     b, perm = wl.permutation(N, K, seed=24)
-    c = run_gpu(plan, a, b, acc)
+    c = run_gpu(plans[variant], a, b, acc)
     assert np.array_equal(c.view(np.uint16), np.ascontiguousarray(a[:, perm]).view(np.uint16))
 
 
 @pytest.mark.parametrize("acc", ["f32", "f16"])
-def test_rank1_exact(plan, acc):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_rank1_exact(plans, variant, acc):
     M, N, K = 260, 264, 600
     a, b, (u, v, w, z) = wl.rank1(M, N, K, seed=25)
-    c = run_gpu(plan, a, b, acc)
+    c = run_gpu(plans[variant], a, b, acc)
     exact = np.outer(u, v).astype(np.float64) * float(np.dot(w, z))
     assert np.array_equal(c.astype(np.float64), exact)
 
@@ -109,23 +122,25 @@ def _sampled_parity(plan, w, acc):
     return st_r, st_c
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("name,acc", [
     ("gemm_4096", "f32"), ("gemm_8192", "f32"), ("gemm_8192", "f16"),
     ("gemm_ragged_3000x5000x4104", "f32"), ("gemm_16384", "f32")])
-def test_workload_sampled(plan, name, acc):
-    st_r, st_c = _sampled_parity(plan, wl.WORKLOADS[name], acc)
-    print(f"{name} {acc}: rows {st_r} cols {st_c}")
+def test_workload_sampled(plans, variant, name, acc):
+    st_r, st_c = _sampled_parity(plans[variant], wl.WORKLOADS[name], acc)
+    print(f"{name} {acc} {variant}: rows {st_r} cols {st_c}")
     if acc == "f16":
         _, pages = read_golden("pages_fp16_acc_error.txt")
         assert st_r["max_abs"] <= pages["atol"] and st_c["max_abs"] <= pages["atol"]
 
 
-def test_16384_all_ones_closed_form(plan):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_16384_all_ones_closed_form(plans, variant):
     M = N = K = 16384
     a = torch.ones((M, K), dtype=torch.float16, device="cuda")
     c = torch.empty((M, N), dtype=torch.float16, device="cuda")
-    plan.run(a, a, c, acc="f32")
-    plan.check_error()
+    plans[variant].run(a, a, c, acc="f32")
+    plans[variant].check_error()
     assert bool((c == 16384.0).all())
 
 
