@@ -22,9 +22,7 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -77,63 +75,88 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+    """SM clock, power and clock-event reasons of one GPU, polled through NVML
+    (read-only queries) on a background thread while the timed region runs.
+    If NVML cannot be loaded the clocks are reported as unavailable."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+    def __init__(self, torch_device, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []          # (sm_mhz, power_w, reasons_mask)
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        try:
+            self._open_nvml(torch_device)
+        except Exception:
+            self._nvml = None
+
+    def _open_nvml(self, dev):
+        import ctypes
+        import threading
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(dev).uuid)
+            ok = nv.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(dev.index or 0),
+                                                       ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint(0)
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self._nvml, self._handle, self._ct, self._threading = nv, h, ctypes, threading
+
+    def _poll(self):
+        ct, nv, h = self._ct, self._nvml, self._handle
+        mhz, mw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        while not self._stop.is_set():
+            a = nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz))
+            b = nv.nvmlDeviceGetPowerUsage(h, ct.byref(mw))
+            c = nv.nvmlDeviceGetCurrentClocksEventReasons(h, ct.byref(rs))
+            if a == 0:
+                self.samples.append((float(mhz.value), mw.value / 1000.0 if b == 0 else None,
+                                     rs.value if c == 0 else 0))
+            self._stop.wait(self.period)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=self.out, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+        if self._nvml is not None:
+            self._stop = self._threading.Event()
+            self._thread = self._threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            time.sleep(0.25)
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
 
     def summary(self):
-        self.out.flush()
-        self.out.seek(0)
-        rows = [ln.strip().split(", ") for ln in self.out if ln.strip()]
-        os.unlink(self.out.name)
-        sm, mx, reasons, power = [], 0.0, set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                mx = max(mx, float(r[2]))
-                power.append(float(r[3]))
-            except ValueError:
-                continue
-            for name, flag in zip(names, r[5:9]):
-                if flag.strip().lower() == "active":
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml" if self._nvml else "unavailable"}
+        sm = [x[0] for x in self.samples]
+        reasons = set()
+        for _, _, mask in self.samples:
+            for bit, name in self.REASONS.items():
+                if mask & bit:
                     reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        # under load = samples above the idle floor
-        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+        power = [x[1] for x in self.samples if x[1] is not None]
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None,
+                "source": "nvml, polled every %.0f ms in the timed region" % (self.period * 1e3)}
 
 
 def cpu_oracle_rate(w, rows_req=0, steps=1, a=None, b=None):
@@ -239,9 +262,7 @@ def run_ours(args):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     launches0 = plan.launch_count
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
-    sampler = ClockSampler(gpu_index)
+    sampler = ClockSampler(dev)
     barrier()
     with sampler:
         t_all0 = torch.cuda.Event(enable_timing=True)
@@ -255,16 +276,12 @@ def run_ours(args):
         barrier()
     launches = plan.launch_count - launches0
     plan.check_error()
-    total_ms = t_all0.elapsed_time(t_all1)
+    total_ms = reduce_max(t_all0.elapsed_time(t_all1), world, dev)
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     clocks = sampler.summary()
 
     flops = float(w.flops)
-    value = world * args.steps * flops / (total_ms * 1e-3) / 1e12
+    value = aggregate_tflops(world, args.steps, flops, total_ms * 1e-3)
     ms_per_step = total_ms / args.steps
     peaks = measured_peaks()
     kernel_ms = statistics.mean(per_launch_ms)
@@ -284,12 +301,8 @@ def run_ours(args):
         t0 = time.perf_counter()
         for _ in range(e_steps):
             plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)
-        dt = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([dt], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": world * e_steps * flops / dt / 1e12, "unit": UNIT,
+        dt = reduce_max(time.perf_counter() - t0, world, dev)
+        e2e = {"value": aggregate_tflops(world, e_steps, flops, dt), "unit": UNIT,
                "h2d_bytes_per_step": int(a_np.nbytes + b_np.nbytes),
                "d2h_bytes_per_step": int(w.M * w.N * 2),
                "ms_per_step": dt / e_steps * 1e3, "steps": e_steps}
@@ -326,15 +339,50 @@ def run_ours(args):
     return 0
 
 
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: a recorded ncu traffic figure is used only
+    while the kernels it was measured on are unchanged."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp16_gemm_04_gb300", "csrc")
+    for path in sorted(glob.glob(os.path.join(csrc, "*.cu*"))):
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def _recorded_traffic(workload, acc, variant):
-    """DRAM bytes per launch from the committed ncu summary of this exact
-    kernel variant and workload, or None if none was recorded."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes (read + write) per launch from the committed ncu summary of
+    this kernel variant and workload, or None if none was recorded for the
+    current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    return d.get(f"{variant}/{workload}/{acc}")
+    e = d.get(f"{variant}/{workload}/{acc}")
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return int(e["dram_bytes_per_launch"])
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(world: int, steps: int, flops_per_step: float, seconds: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of `flops_per_step`
+    in `seconds` (the slowest rank's time)."""
+    return world * steps * flops_per_step / seconds / 1e12
 
 
 def main():
