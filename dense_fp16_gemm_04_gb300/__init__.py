@@ -78,6 +78,9 @@ def load():
             "gemm_plan_last_error_detail": (st, [vp, ctypes.POINTER(ctypes.c_uint32)]),
             "gemm_plan_set_watchdog": (st, [vp, u64, i32]),
             "gemm_plan_set_variant": (st, [vp, i32]),
+            "gemm_plan_set_schedule": (st, [vp, i32]),
+            "gemm_plan_describe": (i32, [vp, i64, i64, i64, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_int64)]),
             "gemm_variant_count": (i32, []),
             "gemm_variant_name": (ctypes.c_char_p, [i32]),
             "gemm_plan_pick_variant": (i32, [vp, i64, i64, i64, ctypes.c_int,
@@ -200,6 +203,19 @@ class Plan:
             variant = variant_names().index(variant)
         _check(self._lib.gemm_plan_set_variant(self._h, int(variant)), "gemm_plan_set_variant")
 
+    def set_schedule(self, mode) -> None:
+        """'auto' (0), 'whole' tiles only (1) or 'streamk' whenever possible (2)."""
+        mode = {"auto": 0, "whole": 1, "streamk": 2}.get(mode, mode)
+        _check(self._lib.gemm_plan_set_schedule(self._h, int(mode)), "gemm_plan_set_schedule")
+
+    def describe(self, M, N, K, acc="f32") -> dict:
+        """How gemm_run would lay out this call on the device."""
+        out = (ctypes.c_int64 * 6)()
+        if self._lib.gemm_plan_describe(self._h, M, N, K, _acc(acc), out) != 0:
+            raise GemmError(1, "gemm_plan_describe")
+        return {"variant": variant_names()[out[0]], "grid_ctas": out[1], "units": out[2],
+                "dp_tiles": out[3], "sk_units": out[4], "sk_iters": out[5]}
+
     def pick_variant(self, M, N, K, acc="f32"):
         grid = ctypes.c_int32(0)
         v = self._lib.gemm_plan_pick_variant(self._h, M, N, K, _acc(acc), ctypes.byref(grid))
@@ -245,16 +261,19 @@ _plans = {}
 _plans_lock = threading.Lock()
 
 
-def default_plan(device=None) -> Plan:
-    """One shared plan per device (created on first use)."""
+def default_plan(device=None, stream=None) -> Plan:
+    """One shared plan per (device, stream), created on first use: work
+    launched through one plan must not overlap on the GPU."""
+    import torch
     if device is None:
-        import torch
         device = torch.cuda.current_device()
     device = int(device)
+    key = (device, _stream_handle(stream) if stream is not None
+           else torch.cuda.current_stream(device).cuda_stream)
     with _plans_lock:
-        p = _plans.get(device)
+        p = _plans.get(key)
         if p is None:
-            p = _plans[device] = Plan(device)
+            p = _plans[key] = Plan(device)
         return p
 
 
@@ -263,7 +282,7 @@ def gemm(a, b, acc="f32", out=None, stream=None, plan: Plan | None = None):
     import torch
     if out is None:
         out = torch.empty((a.shape[0], b.shape[0]), dtype=torch.float16, device=a.device)
-    (plan or default_plan(a.device.index)).run(a, b, out, acc=acc, stream=stream)
+    (plan or default_plan(a.device.index, stream)).run(a, b, out, acc=acc, stream=stream)
     return out
 
 

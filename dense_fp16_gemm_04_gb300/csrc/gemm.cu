@@ -66,6 +66,13 @@ struct gemm_plan_s {
   int device = 0;
   int num_sms = 0;
   int max_pairs = 0;  // CTA pairs of the pair kernel that fit on the device at once
+  // Stream-K workspace, allocated once at plan creation: partial fp32 tiles
+  // (2 slots per unit) and per-tile contribution counters (kept at zero
+  // between launches by the kernel itself).
+  float* sk_ws = nullptr;
+  uint32_t* sk_count = nullptr;
+  size_t sk_count_words = 0;
+  int32_t schedule_mode = 0;  // 0 auto, 1 whole tiles only, 2 stream-K tail whenever possible
   EncodeTiledFn encode = nullptr;
   uint32_t* d_err = nullptr;  // 4-word watchdog record
   uint32_t last_err[4] = {0, 0, 0, 0};
@@ -153,22 +160,64 @@ int64_t tiles_of(const VariantInfo& vi, int64_t M, int64_t N) {
   return ((M + vi.tile_m - 1) / vi.tile_m) * ((N + vi.tile_n - 1) / vi.tile_n);
 }
 
-// Grid in CTAs: one CTA (or pair) per tile up to what fits on the device.
-int grid_for(const VariantInfo& vi, int64_t tiles, int num_sms, int max_pairs) {
-  if (vi.ctas == 2) {
-    const int64_t pairs = tiles < max_pairs ? tiles : max_pairs;
-    return static_cast<int>(2 * pairs);
-  }
-  return static_cast<int>(tiles < num_sms ? tiles : num_sms);
-}
+constexpr int64_t kMinSkIters = 16;  // fewest k-blocks a stream-K unit is given
+constexpr double kSkFixupKb = 2.0;   // cost of a partial-tile fix-up, in k-block times
+constexpr double kSkMinGain = 0.97;  // use the stream-K tail only if it saves >= 3%
 
-int pick_variant(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, int* grid) {
+// How one call is laid out on the device.
+struct Schedule {
+  int variant;
+  int64_t units;      // CTAs or CTA pairs launched
+  int grid;           // CTAs launched
+  int64_t dp_tiles;   // tiles handed out whole
+  int64_t sk_units;   // units sharing the stream-K tail (0 = none)
+  int64_t sk_iters;   // k-blocks in the tail
+};
+
+// Whole tiles are dealt round robin to U persistent units (U = CTA pairs or
+// CTAs that fit at once).  When T tiles are not a multiple of U the last wave
+// runs part-empty; then the last T % U + U tiles (or all of them, T < U)
+// become a stream-K share whose k-blocks are split evenly over the units
+// (each unit runs its share before its whole tiles), if the estimate (in
+// k-block times per unit) says it saves enough.
+Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc) {
   int v = p->forced_variant >= 0 ? p->forced_variant : kVariantPair;
   if (kVariants[v].ctas == 2 && p->max_pairs < 1) v = kVariantSingle;
   const VariantInfo& vi = kVariants[v];
-  (void)K;
-  if (grid) *grid = grid_for(vi, tiles_of(vi, M, N), p->num_sms, p->max_pairs);
-  return v;
+  const int64_t T = tiles_of(vi, M, N);
+  const int64_t KB = (K + 63) / 64;
+  const int64_t U = vi.ctas == 2 ? p->max_pairs : p->num_sms;
+  Schedule s;
+  s.variant = v;
+  s.units = T < U ? T : U;
+  s.dp_tiles = T;
+  s.sk_units = 0;
+  s.sk_iters = 0;
+  const bool allowed = acc == GEMM_ACC_F32 && p->sk_ws && p->sk_count && KB > 0 &&
+                       p->schedule_mode != 1 && (T % U != 0 || p->schedule_mode == 2);
+  if (allowed) {
+    const int64_t sk_tiles = T >= U ? T % U + U : T;
+    const int64_t dp = T - sk_tiles;
+    const int64_t iters = sk_tiles * KB;
+    // Forced mode (testing) lets units take as little as one k-block, so
+    // tiles get many contributors.
+    int64_t usk = iters / (p->schedule_mode == 2 ? 1 : kMinSkIters);
+    if (usk > U) usk = U;
+    const bool fits = static_cast<size_t>(sk_tiles * vi.ctas) <= p->sk_count_words;
+    if (usk >= 2 && fits) {
+      const double t_dp = static_cast<double>((T + U - 1) / U) * KB;
+      const double t_sk = static_cast<double>(dp / U) * KB +
+                          static_cast<double>((iters + usk - 1) / usk) + kSkFixupKb;
+      if (p->schedule_mode == 2 || t_sk < kSkMinGain * t_dp) {
+        s.units = dp > 0 ? U : usk;
+        s.dp_tiles = dp;
+        s.sk_units = usk;
+        s.sk_iters = iters;
+      }
+    }
+  }
+  s.grid = static_cast<int>(s.units * vi.ctas);
+  return s;
 }
 
 template <class Cfg>
@@ -224,9 +273,9 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
     ++p->launches;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
-  int grid = 0;
-  const int v = pick_variant(p, M, N, K, &grid);
-  const VariantInfo& vi = kVariants[v];
+  const Schedule sch = make_schedule(p, M, N, K, acc);
+  const int grid = sch.grid;
+  const VariantInfo& vi = kVariants[sch.variant];
   CUtensorMap ma, mb, mc;
   if (!get_map(p, &ma, A, M, K, vi.box_a_rows, 64) || !get_map(p, &mb, B, N, K, vi.box_b_rows, 64) ||
       !get_map(p, &mc, C, M, N, 32, 64))
@@ -244,6 +293,11 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   args.err = p->d_err;
   args.timeout_ns = p->timeout_ns;
   args.skip_kb = p->skip_kb;
+  args.dp_tiles = static_cast<int32_t>(sch.dp_tiles);
+  args.sk_units = static_cast<int32_t>(sch.sk_units);
+  args.sk_iters = sch.sk_iters;
+  args.sk_ws = p->sk_ws;
+  args.sk_count = p->sk_count;
 
   cudaError_t e;
   if (vi.ctas == 2)
@@ -347,6 +401,21 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     delete p;
     return GEMM_ERR_CUDA;
   }
+  // Stream-K workspace: two 128 x 256 fp32 partial tiles per CTA the device
+  // can hold at once (≈ 39 MB on 152 SMs), and up to two tail tiles per unit.
+  {
+    const size_t ws_floats = 2ull * static_cast<size_t>(sms) * 128ull * 256ull;
+    p->sk_count_words = 4ull * static_cast<size_t>(sms);
+    if (cudaMalloc(&p->sk_ws, ws_floats * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(&p->sk_count, p->sk_count_words * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->sk_count, 0, p->sk_count_words * sizeof(uint32_t)) != cudaSuccess) {
+      if (p->sk_ws) cudaFree(p->sk_ws);
+      if (p->sk_count) cudaFree(p->sk_count);
+      cudaFree(p->d_err);
+      delete p;
+      return GEMM_ERR_OOM;
+    }
+  }
   *out = p;
   return GEMM_OK;
 }
@@ -355,6 +424,8 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t p) {
   if (!p) return GEMM_OK;
   DeviceGuard g(p->device);
   if (p->d_err) cudaFree(p->d_err);
+  if (p->sk_ws) cudaFree(p->sk_ws);
+  if (p->sk_count) cudaFree(p->sk_count);
   if (p->dA) cudaFree(p->dA);
   if (p->dB) cudaFree(p->dB);
   if (p->dC) cudaFree(p->dC);
@@ -369,6 +440,25 @@ gemm_status_t gemm_plan_set_watchdog(gemm_plan_t p, uint64_t timeout_ns, int32_t
   return GEMM_OK;
 }
 
+gemm_status_t gemm_plan_set_schedule(gemm_plan_t p, int32_t mode) {
+  if (!p || mode < 0 || mode > 2) return GEMM_ERR_INVALID_ARG;
+  p->schedule_mode = mode;
+  return GEMM_OK;
+}
+
+int32_t gemm_plan_describe(gemm_plan_t p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
+                           int64_t out[6]) {
+  if (!p || !out || check_shape(M, N, K, acc) != GEMM_OK) return -1;
+  const Schedule s = make_schedule(p, M, N, K, acc);
+  out[0] = s.variant;
+  out[1] = s.grid;
+  out[2] = s.units;
+  out[3] = s.dp_tiles;
+  out[4] = s.sk_units;
+  out[5] = s.sk_iters;
+  return 0;
+}
+
 gemm_status_t gemm_plan_set_variant(gemm_plan_t p, int32_t v) {
   if (!p || v < -1 || v >= kNumVariants) return GEMM_ERR_INVALID_ARG;
   p->forced_variant = v;
@@ -378,10 +468,9 @@ gemm_status_t gemm_plan_set_variant(gemm_plan_t p, int32_t v) {
 int32_t gemm_plan_pick_variant(gemm_plan_t p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
                                int32_t* grid_ctas) {
   if (!p || check_shape(M, N, K, acc) != GEMM_OK) return -1;
-  int grid = 0;
-  int v = pick_variant(p, M, N, K, &grid);
-  if (grid_ctas) *grid_ctas = grid;
-  return v;
+  const Schedule s = make_schedule(p, M, N, K, acc);
+  if (grid_ctas) *grid_ctas = s.grid;
+  return s.variant;
 }
 
 uint64_t gemm_plan_launch_count(gemm_plan_t p) { return p ? p->launches : 0; }
@@ -416,6 +505,10 @@ gemm_status_t gemm_plan_check_error(gemm_plan_t p) {
   if (rec[0] == 0) return GEMM_OK;
   std::memcpy(p->last_err, rec, sizeof(rec));
   if (cudaMemset(p->d_err, 0, sizeof(rec)) != cudaSuccess) return GEMM_ERR_CUDA;
+  // A launch that gave up may have left stream-K counters mid-count.
+  if (p->sk_count &&
+      cudaMemset(p->sk_count, 0, p->sk_count_words * sizeof(uint32_t)) != cudaSuccess)
+    return GEMM_ERR_CUDA;
   return static_cast<gemm_status_t>(rec[0]);
 }
 
@@ -583,6 +676,11 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   args.err = d.scratch;
   args.timeout_ns = kDefaultTimeoutNs;
   args.skip_kb = -1;
+  args.dp_tiles = args.num_tiles;  // whole tiles only: no stream-K workspace here
+  args.sk_units = 0;
+  args.sk_iters = 0;
+  args.sk_ws = nullptr;
+  args.sk_count = nullptr;
   const int grid = args.num_tiles < d.num_sms ? args.num_tiles : d.num_sms;
   // The watchdog record must start at zero; the array keeps the last call's
   // contents, so clear it on the caller's stream before the launch.

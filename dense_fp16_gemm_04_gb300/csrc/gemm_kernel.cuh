@@ -59,6 +59,83 @@ struct GemmArgs {
   uint32_t* err;        // device watchdog record, 4 words
   uint64_t timeout_ns;  // longest allowed single wait
   int32_t skip_kb;      // fault injection, -1 = off
+  // Schedule: tiles [0, dp_tiles) are dealt out whole, round robin over the
+  // units (CTAs or CTA pairs).  The remaining tiles form the stream-K tail:
+  // their sk_iters = (num_tiles - dp_tiles) * num_kb k-blocks are cut into
+  // sk_units equal contiguous ranges, so a tail tile may be shared by several
+  // units, each accumulating a k-range of it.
+  int32_t dp_tiles;
+  int32_t sk_units;     // 0 = no stream-K tail
+  int64_t sk_iters;
+  float* sk_ws;         // partial accumulators: [unit][2 slots][CTA of unit][128 x 256] fp32
+  uint32_t* sk_count;   // per tail tile and CTA of the tile: contributions so far (self-resetting)
+};
+
+// One piece of work for a unit: k-blocks [kb0, kb1) of one output tile.
+struct WorkItem {
+  int32_t tile;        // linear tile index, before rastering
+  int32_t kb0, kb1;
+  int32_t sk_tile;     // index in the stream-K tail, -1 for a whole tile
+  int32_t splits;      // units contributing to this tile (1: no fix-up)
+  int32_t first_unit;  // first contributing unit (stream-K tail only)
+};
+
+// The work list of one unit, identical in every role of the unit's CTAs:
+// first its share of the stream-K tail, then its whole tiles.
+struct Sched {
+  int32_t unit, units, dp_tiles, num_kb, sk_units;
+  int64_t sk_iters;
+  int32_t next_dp;
+  int64_t x, x_end;  // this unit's remaining range of tail k-blocks
+
+  __device__ __forceinline__ Sched(const GemmArgs& a, int32_t unit_, int32_t units_)
+      : unit(unit_), units(units_), dp_tiles(a.dp_tiles), num_kb(a.num_kb),
+        sk_units(a.sk_units), sk_iters(a.sk_iters), next_dp(unit_), x(0), x_end(0) {
+    if (sk_units > 0 && unit < sk_units) {
+      x = bound(unit);
+      x_end = bound(unit + 1);
+    }
+  }
+  // First tail k-block of unit u.
+  __device__ __forceinline__ int64_t bound(int64_t u) const { return u * sk_iters / sk_units; }
+  // The unit whose range holds tail k-block `it` (the largest u with bound(u) <= it).
+  __device__ __forceinline__ int32_t unit_of(int64_t it) const {
+    return static_cast<int32_t>(((it + 1) * sk_units - 1) / sk_iters);
+  }
+  // Workspace slot unit u uses for tail tile t: 0 if t is the first tile its
+  // range touches, else 1 (only a range's first and last tiles can be partial).
+  __device__ __forceinline__ int32_t slot_of(int32_t u, int32_t t) const {
+    return static_cast<int32_t>(bound(u) / num_kb) == t ? 0 : 1;
+  }
+  // Stream-K pieces come first and whole tiles after them: the fix-up of a
+  // shared tile (reading the other units' partials) then overlaps the main
+  // loop of a later whole tile instead of ending the kernel.
+  __device__ __forceinline__ bool next(WorkItem& w) {
+    if (x >= x_end && next_dp < dp_tiles) {
+      w.tile = next_dp;
+      w.kb0 = 0;
+      w.kb1 = num_kb;
+      w.sk_tile = -1;
+      w.splits = 1;
+      w.first_unit = unit;
+      next_dp += units;
+      return true;
+    }
+    if (x < x_end) {
+      const int32_t t = static_cast<int32_t>(x / num_kb);
+      const int64_t t0 = static_cast<int64_t>(t) * num_kb, t1 = t0 + num_kb;
+      const int64_t e = x_end < t1 ? x_end : t1;
+      w.tile = dp_tiles + t;
+      w.kb0 = static_cast<int32_t>(x - t0);
+      w.kb1 = static_cast<int32_t>(e - t0);
+      w.sk_tile = t;
+      w.first_unit = unit_of(t0);
+      w.splits = unit_of(t1 - 1) - w.first_unit + 1;
+      x = e;
+      return true;
+    }
+    return false;
+  }
 };
 
 // Tile configuration.  kCtas CTAs cooperate on one tile of kTileM x kBN.
@@ -86,7 +163,9 @@ struct GemmCfg {
   static constexpr int kNumBars = 2 * kStages + 5;  // full, empty, tmem_full[2], tmem_empty[2], mma_done
   static constexpr int kOffSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffSlot + 4;
-  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
+  static constexpr int kOffFlag = kOffAbort + 4;           // stream-K "last contributor" flag
+  static constexpr int kSmemBytes = kOffFlag + 4 + 1024;   // + slack to align the base to 1024
+  static constexpr int kPartialFloats = kBM * kBN;         // one CTA's share of a partial tile
   static constexpr int kTmemCols = 2 * kBN;
   static constexpr int kThreads = 192;
   static constexpr uint32_t kIdesc = ptx::idesc_f16(kTileM, kBN, !kAccF16);
@@ -217,21 +296,24 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer --
+      Sched sched(args, unit, units);
+      WorkItem wi;
       int stage = 0;
       uint32_t phase = 0;
       int64_t fills = 0;
       bool ok = true;
-      for (int32_t tile = unit; ok && tile < args.num_tiles; tile += units) {
+      bool first_item = true;
+      while (ok && sched.next(wi)) {
         int32_t mb, nb;
-        raster(tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
+        raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
         const int32_t a_row = mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM;
         const int32_t b_row = nb * Cfg::kBN + static_cast<int32_t>(rank) * Cfg::kBRows;
-        for (int32_t kb = 0; kb < args.num_kb; ++kb) {
-          if (!wait_bar<kPair>(bar_empty(stage), phase ^ 1u, w, kSiteEmpty, tile)) {
+        for (int32_t kb = wi.kb0; kb < wi.kb1; ++kb) {
+          if (!wait_bar<kPair>(bar_empty(stage), phase ^ 1u, w, kSiteEmpty, wi.tile)) {
             ok = false;
             break;
           }
-          const bool skip = args.skip_kb == kb && tile == unit && unit == 0 && rank == 0;
+          const bool skip = args.skip_kb == kb && first_item && unit == 0 && rank == 0;
           if (!skip) {
             if constexpr (kPair) {
               // Both CTAs' bytes are counted on the leader's full barrier; the
@@ -252,6 +334,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             phase ^= 1u;
           }
         }
+        first_item = false;
       }
       // Drain: the last min(S, fills) fills may still be in use.  Normally
       // wait until the MMA issuer has released each of them, so no tcgen05
@@ -271,21 +354,23 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ------------------------------------------------------- MMA issuer --
+      Sched sched(args, unit, units);
+      WorkItem wi;
       int stage = 0;
       uint32_t phase = 0;
       int32_t acc_iter = 0;
       bool ok = true;
-      for (int32_t tile = unit; ok && tile < args.num_tiles; tile += units) {
+      while (ok && sched.next(wi)) {
         const int buf = acc_iter & 1;
         const uint32_t use_par = static_cast<uint32_t>((acc_iter >> 1) & 1);
-        if (!wait_bar<kPair>(bar_tempty(buf), use_par ^ 1u, w, kSiteTmemEmpty, tile)) {
+        if (!wait_bar<kPair>(bar_tempty(buf), use_par ^ 1u, w, kSiteTmemEmpty, wi.tile)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kBN);
-        for (int32_t kb = 0; kb < args.num_kb; ++kb) {
-          if (!wait_bar<kPair>(bar_full(stage), phase, w, kSiteFull, tile)) {
+        for (int32_t kb = wi.kb0; kb < wi.kb1; ++kb) {
+          if (!wait_bar<kPair>(bar_full(stage), phase, w, kSiteFull, wi.tile)) {
             ok = false;
             break;
           }
@@ -294,9 +379,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const uint64_t b_desc = ptx::sw128_kmajor_desc(sB(stage));
 #pragma unroll
           for (int k = 0; k < Cfg::kBK / 16; ++k) {
-            // +32 bytes along K per 16-element step, inside the swizzled row
+            // +32 bytes along K per 16-element step, inside the swizzled row;
+            // the first step of the item overwrites the accumulator.
             ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
-                                     (kb | k) != 0 ? 1u : 0u);
+                                     (kb != wi.kb0 || k != 0) ? 1u : 0u);
           }
           if constexpr (kPair)
             ptx::mma_commit_pair(bar_empty(stage), 0x3);
@@ -325,51 +411,132 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue --
     const int q = warp & 3;  // this warp may touch TMEM lanes 32q .. 32q+31 only
+    const int row_in_cta = q * 32 + lane;
     const uint32_t stage_base = sb + Cfg::kOffEpi + static_cast<uint32_t>(q * 2 * Cfg::kEpiBufBytes);
     // tmem_empty lives in the leader CTA: every epilogue warp of the pair
     // arrives there.
     const uint32_t tempty_bar0 = kPair ? ptx::mapa(bar_tempty(0), 0) : bar_tempty(0);
+    volatile uint32_t* last_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffFlag);
+    // This CTA's share of unit u's partial tile in slot `slot`.
+    auto partial = [&](int32_t u, int32_t slot) {
+      return args.sk_ws + (static_cast<size_t>(u * 2 + slot) * Cfg::kCtas + rank) *
+                              static_cast<size_t>(Cfg::kPartialFloats);
+    };
+    Sched sched(args, unit, units);
+    WorkItem wi;
     uint32_t stores = 0;
     int32_t acc_iter = 0;
-    for (int32_t tile = unit; tile < args.num_tiles; tile += units) {
+    while (sched.next(wi)) {
       int32_t mb, nb;
-      raster(tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
+      raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
       const int buf = acc_iter & 1;
       const uint32_t use_par = static_cast<uint32_t>((acc_iter >> 1) & 1);
+      ++acc_iter;
       int ok = 1;
-      if (lane == 0) ok = wait_bar<kPair>(bar_tfull(buf), use_par, w, kSiteTmemFull, tile) ? 1 : 0;
+      if (lane == 0) ok = wait_bar<kPair>(bar_tfull(buf), use_par, w, kSiteTmemFull, wi.tile) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      // All epilogue warps take the same decision, so none is left waiting at
+      // a barrier below for a warp that gave up.
+      if (!ptx::named_barrier_and(1, 32 * Cfg::kEpiWarps, ok != 0)) break;
       ptx::tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * Cfg::kBN);
       const int32_t row0 = mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM + q * 32;
+      const bool split = !Cfg::kAccF16 && wi.splits > 1;
+      if (split) {
+        // Stream-K tail tile shared with other units.  (a) Park this unit's
+        // partial accumulator (fp32) in its workspace slot and give the TMEM
+        // buffer back.
+        // Partial tile layout [column / 4][row][column % 4]: for a fixed group
+        // of four columns the warp's 32 rows are 512 contiguous bytes, so every
+        // store (and the fix-up's loads) is one fully used burst.
+        float* own = partial(unit, sched.slot_of(unit, wi.sk_tile)) +
+                     static_cast<size_t>(row_in_cta) * 4;
+#pragma unroll 1
+        for (int c = 0; c < Cfg::kBN / 32; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c * 32, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            ptx::st_global_v4(own + static_cast<size_t>(c * 8 + j) * (Cfg::kBM * 4), v[4 * j],
+                              v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair)
+            ptx::mbar_arrive_cluster(tempty_bar0 + 8u * buf);
+          else
+            ptx::mbar_arrive(tempty_bar0 + 8u * buf);
+        }
+        // (b) Count this contribution.  Whoever brings the count to `splits`
+        // holds the last piece: it resets the counter for the next launch and
+        // finishes the tile.  Nobody waits for anybody.
+        __threadfence();
+        ptx::named_barrier_sync(1, 32 * Cfg::kEpiWarps);
+        if (threadIdx.x == 64) {
+          uint32_t* cnt = args.sk_count + static_cast<size_t>(wi.sk_tile) * Cfg::kCtas + rank;
+          const uint32_t before = atomicAdd(cnt, 1u);
+          const bool last = before == static_cast<uint32_t>(wi.splits - 1);
+          if (last) *cnt = 0u;
+          *last_flag = last ? 1u : 0u;
+        }
+        ptx::named_barrier_sync(1, 32 * Cfg::kEpiWarps);
+        if (*last_flag == 0u) continue;
+        __threadfence();
+      }
 #pragma unroll 1
       for (int c = 0; c < Cfg::kBN / 64; ++c) {
         uint32_t packed[32];
-        if constexpr (Cfg::kAccF16) {
-          ptx::tmem_ld_32x32b_x32_pack16(t_row + c * 64, packed);
-          ptx::tmem_wait_ld();
-        } else {
-          uint32_t v0[32], v1[32];
-          ptx::tmem_ld_32x32b_x32(t_row + c * 64, v0);
-          ptx::tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
-          ptx::tmem_wait_ld();
+        if (split) {
+          // (c) The tile's value: the contributors' partials summed in unit
+          // order, so the result does not depend on who finished last.
+          float acc[64];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            packed[i] = pack_half2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
-            packed[16 + i] = pack_half2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+          for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+          for (int32_t j = 0; j < wi.splits; ++j) {
+            const int32_t u = wi.first_unit + j;
+            const float* src = partial(u, sched.slot_of(u, wi.sk_tile)) +
+                               static_cast<size_t>(row_in_cta) * 4 +
+                               static_cast<size_t>(c * 16) * (Cfg::kBM * 4);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float4 v = ptx::ld_global_cg_v4(src + static_cast<size_t>(i) * (Cfg::kBM * 4));
+              acc[4 * i] += v.x;
+              acc[4 * i + 1] += v.y;
+              acc[4 * i + 2] += v.z;
+              acc[4 * i + 3] += v.w;
+            }
           }
-        }
-        if (c == Cfg::kBN / 64 - 1) {
-          // The whole accumulator buffer is in registers: hand it back.
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (kPair)
-              ptx::mbar_arrive_cluster(tempty_bar0 + 8u * buf);
-            else
-              ptx::mbar_arrive(tempty_bar0 + 8u * buf);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) packed[i] = pack_half2(acc[2 * i], acc[2 * i + 1]);
+        } else {
+          if constexpr (Cfg::kAccF16) {
+            ptx::tmem_ld_32x32b_x32_pack16(t_row + c * 64, packed);
+            ptx::tmem_wait_ld();
+          } else {
+            uint32_t v0[32], v1[32];
+            ptx::tmem_ld_32x32b_x32(t_row + c * 64, v0);
+            ptx::tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              packed[i] = pack_half2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+              packed[16 + i] =
+                  pack_half2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+            }
+          }
+          if (c == Cfg::kBN / 64 - 1) {
+            // The whole accumulator buffer is in registers: hand it back.
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (kPair)
+                ptx::mbar_arrive_cluster(tempty_bar0 + 8u * buf);
+              else
+                ptx::mbar_arrive(tempty_bar0 + 8u * buf);
+            }
           }
         }
         const uint32_t sbuf = stage_base + (stores & 1u) * Cfg::kEpiBufBytes;
@@ -394,7 +561,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         stores = __shfl_sync(0xffffffffu, stores, 0);
       }
-      ++acc_iter;
     }
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();

@@ -13,9 +13,10 @@
  * Epilogue", section "The Register Budget Problem"), and written as fp16
  * rounded to nearest even.
  *
- * Ownership: the caller owns every buffer.  The library owns only the plan
- * (a few bytes of device memory for the watchdog record, and, for
- * gemm_run_host, device staging buffers it grows on demand).
+ * Ownership: the caller owns every buffer.  The library owns only the plan:
+ * the device watchdog record, a stream-K workspace of about 0.25 MB per SM
+ * (allocated when the plan is created), and, for gemm_run_host, device staging
+ * buffers it grows on demand.
  *
  * Errors: every entry point returns a gemm_status_t.  Argument checks run on
  * the host before any launch, so a rejected call writes nothing.  A kernel
@@ -23,8 +24,10 @@
  * not hang: it records GEMM_ERR_TIMEOUT on the device, frees its tensor
  * memory and returns; gemm_plan_check_error reports it.
  *
- * Threads: a plan may be used by one host thread at a time.  Different plans
- * are independent.
+ * Threads and streams: a plan may be used by one host thread at a time, and
+ * work launched through one plan must not run concurrently on the GPU (its
+ * calls share the plan's workspace): give each stream its own plan.
+ * Different plans are independent.
  */
 #ifndef GB300_GEMM_H_
 #define GB300_GEMM_H_
@@ -119,6 +122,21 @@ GEMM_API gemm_status_t gemm_plan_last_error_detail(gemm_plan_t plan, uint32_t de
  *   the context usable. */
 GEMM_API gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout_ns,
                                      int32_t skip_k_block);
+
+/* Work schedule: 0 = automatic (default); 1 = whole tiles only; 2 = use the
+ * stream-K tail whenever the shape allows it, down to one k-block per CTA
+ * (testing).  With the tail, the
+ * k-blocks of the last tiles are shared out evenly over all CTAs and partial
+ * fp32 tiles are summed in a fixed order in the plan's workspace (so results
+ * stay deterministic); fp16 accumulation always uses whole tiles. */
+GEMM_API gemm_status_t gemm_plan_set_schedule(gemm_plan_t plan, int32_t mode);
+
+/* How gemm_run would lay out this call: out[0] variant, out[1] CTAs launched,
+ * out[2] units (CTAs or CTA pairs), out[3] tiles handed out whole, out[4]
+ * units sharing the stream-K tail (0 = none), out[5] k-blocks in the tail.
+ * Returns 0, or -1 on a rejected shape. */
+GEMM_API int32_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
+                                    gemm_acc_t acc, int64_t out[6]);
 
 /* Override the kernel variant chosen for a shape (-1 = automatic).  The
  * variants are listed by gemm_variant_name(0 .. gemm_variant_count()-1). */

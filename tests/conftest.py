@@ -94,6 +94,22 @@ def plan():
 
 
 @pytest.fixture(scope="session")
+def plans_streamk():
+    """One plan per kernel variant, forced to use the stream-K tail whenever
+    the shape allows it."""
+    import dense_fp16_gemm_04_gb300 as g
+    g.build()
+    ps = {}
+    for name in VARIANTS:
+        ps[name] = g.Plan(0)
+        ps[name].set_variant(name)
+        ps[name].set_schedule("streamk")
+    yield ps
+    for p in ps.values():
+        p.close()
+
+
+@pytest.fixture(scope="session")
 def plans():
     """One plan per kernel variant, each forced to that variant."""
     import dense_fp16_gemm_04_gb300 as g
