@@ -91,13 +91,16 @@ GEMM_API gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, 
                        int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
                        void* stream);
 
-/* Same product on HOST buffers: copies A and B to device staging buffers owned
- * by the plan (grown with cudaMalloc on first use of a larger shape), runs
- * gemm_run on `stream`, copies C back and synchronizes `stream` before
- * returning.  A, B, C are host pointers (pinned memory gives full copy
- * bandwidth; pageable memory works but is slower).  Same shape and
- * alignment rules as gemm_run (host pointers need no particular alignment).
- * Returns the watchdog status of the run as well. */
+/* Same product on HOST buffers, synchronous: copies B and then row chunks of
+ * A to device staging buffers owned by the plan (grown with cudaMalloc on
+ * first use of a larger shape), multiplies each chunk as soon as it has
+ * arrived and copies its rows of C back while later chunks are still in
+ * flight (three internal streams, created on first use).  The work starts
+ * after everything already queued on `stream`; the call returns when C is
+ * filled.  A, B, C are host pointers (pinned memory gives full copy
+ * bandwidth and the overlap; pageable memory works but is slower).  Same
+ * shape and alignment rules as gemm_run (host pointers need no particular
+ * alignment).  Returns the watchdog status of the run as well. */
 GEMM_API gemm_status_t gemm_run_host(gemm_plan_t plan, const void* A, const void* B, void* C,
                             int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
                             void* stream);

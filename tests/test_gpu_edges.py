@@ -105,19 +105,36 @@ def test_side_stream(plan):
 
 
 @pytest.mark.parametrize("acc", ["f32", "f16"])
-def test_host_entry_point_matches_device_entry_point(plan, acc):
+def test_host_entry_point_matches_device_entry_point(acc):
+    """gemm_run_host pipelines row chunks; with whole-tile schedules every tile
+    is computed exactly as by gemm_run, so the results agree bit for bit."""
+    p = g.Plan(0)
+    p.set_schedule("whole")
     M, N, K = 700, 1032, 520
     a, b = wl.draw(M, N, K, seed=34)
-    dev = run_gpu(plan, a, b, acc)
+    dev = run_gpu(p, a, b, acc)
     ha = torch.from_numpy(a).pin_memory()
     hb = torch.from_numpy(b).pin_memory()
     hc = torch.empty((M, N), dtype=torch.float16).pin_memory()
-    plan.run_host(ha, hb, hc, acc=acc)
+    p.run_host(ha, hb, hc, acc=acc)
     assert np.array_equal(hc.numpy().view(np.uint16), dev.view(np.uint16))
     # pageable numpy buffers work too
     out = np.empty((M, N), np.float16)
-    plan.run_host(a, b, out, acc=acc)
+    p.run_host(a, b, out, acc=acc)
     assert np.array_equal(out.view(np.uint16), dev.view(np.uint16))
+    p.close()
+
+
+def test_host_entry_point_ragged_many_chunks(plan):
+    """A ragged shape split into several row chunks (and, per chunk, whatever
+    schedule the plan picks) against the oracle on sampled rows."""
+    w = wl.WORKLOADS["gemm_ragged_3000x5000x4104"]
+    a, b = wl.inputs_for(w)
+    hc = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+    plan.run_host(torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory(), hc)
+    rows = wl.sample_indices(w.M, 64, 71)
+    got = hc.numpy()[rows].astype(np.float64)
+    assert_close(got, oracle.gemm_rows_f64(a, b, rows), "f32", "run_host ragged")
 
 
 def test_gemm_convenience_wrapper(plan):
