@@ -32,6 +32,10 @@ using PairF32 = GemmCfg<2, 6, false>;    // CTA pair, 256 x 256 tile, 6 stages
 using PairF16 = GemmCfg<2, 6, true>;
 using SingleF32 = GemmCfg<1, 4, false>;  // one CTA, 128 x 256 tile, 4 stages
 using SingleF16 = GemmCfg<1, 4, true>;
+using Pair128F32 = GemmCfg<2, 8, false, 128>;   // CTA pair, 256 x 128 tile, 8 stages
+using Pair128F16 = GemmCfg<2, 8, true, 128>;
+using Single64F32 = GemmCfg<1, 8, false, 64>;   // one CTA, 128 x 64 tile, 8 stages
+using Single64F16 = GemmCfg<1, 8, true, 64>;
 
 struct VariantInfo {
   const char* name;
@@ -43,10 +47,14 @@ struct VariantInfo {
 
 constexpr int kVariantPair = 0;
 constexpr int kVariantSingle = 1;
-constexpr int kNumVariants = 2;
+constexpr int kVariantPair128 = 2;
+constexpr int kVariantSingle64 = 3;
+constexpr int kNumVariants = 4;
 constexpr VariantInfo kVariants[kNumVariants] = {
     {"tc_pair_256x256_s6", 2, 256, 256, 128, 128},
     {"tc_single_128x256_s4", 1, 128, 256, 128, 256},
+    {"tc_pair_256x128_s8", 2, 256, 128, 128, 64},
+    {"tc_single_128x64_s8", 1, 128, 64, 128, 64},
 };
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s for any single wait
@@ -188,10 +196,11 @@ struct Schedule {
 
 // Whole tiles are dealt round robin to U persistent units (U = CTA pairs or
 // CTAs that fit at once).  When T tiles are not a multiple of U the last wave
-// runs part-empty; then the last T % U + U tiles (or all of them, T < U)
-// become a stream-K share whose k-blocks are split evenly over the units
-// (each unit runs its share before its whole tiles), if the estimate (in
-// k-block times per unit) says it saves enough.
+// runs part-empty; then the last T % U + U tiles become a stream-K share
+// whose k-blocks are split evenly over the units (each unit runs its share
+// before its whole tiles), if the estimate (in k-block times per unit) says
+// it saves enough.  The testing mode 2 forces the share on any shape
+// (all tiles when T < 2U).
 Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc) {
   int v = p->forced_variant >= 0 ? p->forced_variant : kVariantPair;
   if (kVariants[v].ctas == 2 && p->max_pairs < 1) v = kVariantSingle;
@@ -205,8 +214,13 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
   s.dp_tiles = T;
   s.sk_units = 0;
   s.sk_iters = 0;
+  // The share pays only when whole tiles follow it (T >= 2U): the partial-tile
+  // fix-ups then overlap those tiles' main loops.  With nothing after it, the
+  // fix-ups end the kernel and cost more than the part-empty wave they save
+  // (measured: 1024 x 8192 x 8192 at 119 us with the share, 88 us without).
   const bool allowed = acc == GEMM_ACC_F32 && p->sk_ws && p->sk_count && KB > 0 &&
-                       p->schedule_mode != 1 && (T % U != 0 || p->schedule_mode == 2);
+                       p->schedule_mode != 1 &&
+                       ((T % U != 0 && T >= 2 * U) || p->schedule_mode == 2);
   if (allowed) {
     const int64_t sk_tiles = T >= U ? T % U + U : T;
     const int64_t dp = T - sk_tiles;
@@ -215,6 +229,9 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
     // tiles get many contributors.
     int64_t usk = iters / (p->schedule_mode == 2 ? 1 : kMinSkIters);
     if (usk > U) usk = U;
+    // At most about two contributors per tile: the last one reads the others'
+    // partial tiles, and that read grows with their number.
+    if (p->schedule_mode != 2 && usk > 2 * sk_tiles) usk = 2 * sk_tiles;
     const bool fits = static_cast<size_t>(sk_tiles * vi.ctas) <= p->sk_count_words;
     if (usk >= 2 && fits) {
       const double t_dp = static_cast<double>((T + U - 1) / U) * KB;
@@ -311,13 +328,25 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   args.sk_ws = p->sk_ws;
   args.sk_count = p->sk_count;
 
+  const bool f32 = acc == GEMM_ACC_F32;
   cudaError_t e;
-  if (vi.ctas == 2)
-    e = acc == GEMM_ACC_F32 ? launch_gemm<PairF32>(ma, mb, mc, args, grid, stream)
-                            : launch_gemm<PairF16>(ma, mb, mc, args, grid, stream);
-  else
-    e = acc == GEMM_ACC_F32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, stream)
-                            : launch_gemm<SingleF16>(ma, mb, mc, args, grid, stream);
+  switch (sch.variant) {
+    case kVariantPair:
+      e = f32 ? launch_gemm<PairF32>(ma, mb, mc, args, grid, stream)
+              : launch_gemm<PairF16>(ma, mb, mc, args, grid, stream);
+      break;
+    case kVariantPair128:
+      e = f32 ? launch_gemm<Pair128F32>(ma, mb, mc, args, grid, stream)
+              : launch_gemm<Pair128F16>(ma, mb, mc, args, grid, stream);
+      break;
+    case kVariantSingle64:
+      e = f32 ? launch_gemm<Single64F32>(ma, mb, mc, args, grid, stream)
+              : launch_gemm<Single64F16>(ma, mb, mc, args, grid, stream);
+      break;
+    default:
+      e = f32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, stream)
+              : launch_gemm<SingleF16>(ma, mb, mc, args, grid, stream);
+  }
   ++p->launches;
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -396,13 +425,18 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
   }
   p->encode = reinterpret_cast<EncodeTiledFn>(fn);
   if (set_smem_attr<SingleF32>() != cudaSuccess || set_smem_attr<SingleF16>() != cudaSuccess ||
-      set_smem_attr<PairF32>() != cudaSuccess || set_smem_attr<PairF16>() != cudaSuccess) {
+      set_smem_attr<PairF32>() != cudaSuccess || set_smem_attr<PairF16>() != cudaSuccess ||
+      set_smem_attr<Pair128F32>() != cudaSuccess || set_smem_attr<Pair128F16>() != cudaSuccess ||
+      set_smem_attr<Single64F32>() != cudaSuccess || set_smem_attr<Single64F16>() != cudaSuccess) {
     delete p;
     return GEMM_ERR_CUDA;
   }
   {
-    const int a = max_active_pairs<PairF32>(), b = max_active_pairs<PairF16>();
-    p->max_pairs = a < b ? a : b;
+    int m = max_active_pairs<PairF32>();
+    for (int n : {max_active_pairs<PairF16>(), max_active_pairs<Pair128F32>(),
+                  max_active_pairs<Pair128F16>()})
+      m = n < m ? n : m;
+    p->max_pairs = m;
   }
   if (cudaMalloc(&p->d_err, 4 * sizeof(uint32_t)) != cudaSuccess) {
     delete p;

@@ -3,13 +3,14 @@
 //   C[M,N] = A[M,K] x B[N,K]^T, fp16 in, fp32 or fp16 accumulate, fp16 out
 //   (tilus "A Minimal Hopper Matmul", section "Block Tiling").
 //
-// One template, two forms:
-//   kCtas = 1  one CTA per SM owns a 128 x 256 output tile;
-//   kCtas = 2  a cluster of two CTAs on neighbouring SMs owns a 256 x 256
-//              tile: each CTA loads its 128 rows of A and half (128 rows) of
-//              B, and one thread of the leader CTA issues
+// One template, two forms (tile width kBN = 64, 128 or 256 columns):
+//   kCtas = 1  one CTA per SM owns a 128 x kBN output tile;
+//   kCtas = 2  a cluster of two CTAs on neighbouring SMs owns a 256 x kBN
+//              tile: each CTA loads its 128 rows of A and half of the tile's
+//              rows of B, and one thread of the leader CTA issues
 //              tcgen05.mma.cta_group::2 (M = 256) over both CTAs' shared
-//              memory, so every SM stages a third less operand data per FLOP.
+//              memory, so every SM stages a third less operand data per FLOP
+//              (at kBN = 256).
 //
 // CTAs (or pairs) are persistent and walk the tiles with a static stride over
 // a grouped raster.  Inside a CTA the work is split by warp, after the
@@ -23,7 +24,7 @@
 //   warps 2..5       epilogue: tcgen05.ld the accumulator, round to fp16,
 //                    stage through swizzled shared memory, TMA-store.
 //
-// The accumulator is double-buffered in TMEM (2 x 256 columns), so the
+// The accumulator is double-buffered in TMEM (2 x kBN columns), so the
 // epilogue of one tile overlaps the main loop of the next; tmem_full /
 // tmem_empty barriers hand the buffers back and forth.
 //
@@ -139,11 +140,11 @@ struct Sched {
 };
 
 // Tile configuration.  kCtas CTAs cooperate on one tile of kTileM x kBN.
-template <int kCtas_, int kStages_, bool kAccF16_>
+template <int kCtas_, int kStages_, bool kAccF16_, int kBN_ = 256>
 struct GemmCfg {
   static constexpr int kCtas = kCtas_;
   static constexpr int kBM = 128;                 // rows of C per CTA
-  static constexpr int kBN = 256;                 // columns of C per tile
+  static constexpr int kBN = kBN_;                // columns of C per tile
   static constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle row)
   static constexpr int kTileM = kBM * kCtas;      // rows of C per tile
   static constexpr int kBRows = kBN / kCtas;      // rows of B each CTA loads
@@ -171,7 +172,10 @@ struct GemmCfg {
   static constexpr uint32_t kIdesc = ptx::idesc_f16(kTileM, kBN, !kAccF16);
 
   static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair");
-  static_assert(kTmemCols == 512, "two 256-column accumulators fill TMEM");
+  static_assert(kBN == 64 || kBN == 128 || kBN == 256, "tile width 64, 128 or 256");
+  static_assert(kBRows >= 8 && kBRows % 8 == 0, "B rows per CTA: whole 8-row swizzle atoms");
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
+                "TMEM is allocated in powers of two from 32 to 512 columns");
   static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory per CTA");
   static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1024 B alignment");
   // Barriers sit after every TMA destination, never inside one (tilus "A

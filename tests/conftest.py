@@ -80,7 +80,8 @@ def assert_close(got, ref, acc, what=""):
 
 # Kernel variants of the library, in its table order (checked against the
 # library by test_abi_host.py::test_variant_table).
-VARIANTS = ["tc_pair_256x256_s6", "tc_single_128x256_s4"]
+VARIANTS = ["tc_pair_256x256_s6", "tc_single_128x256_s4", "tc_pair_256x128_s8",
+            "tc_single_128x64_s8"]
 
 
 @pytest.fixture(scope="session")

@@ -70,4 +70,6 @@ def test_auto_schedule_uses_the_tail_on_quantized_waves(plan):
     d = plan.describe(8192, 8192, 8192, "f16")
     assert d["sk_units"] == 0           # fp16 accumulation keeps whole tiles
     d = plan.describe(512, 512, 512)
-    assert d["sk_units"] == 0           # 8 k-blocks per tile: too little to share
+    assert d["sk_units"] == 0           # fewer tiles than units: whole tiles
+    d = plan.describe(1024, 8192, 8192)
+    assert d["sk_units"] == 0           # no whole wave would follow the share
