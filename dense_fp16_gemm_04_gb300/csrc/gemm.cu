@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
 
 #include "gemm.h"
 #include "gemm_kernel.cuh"
@@ -36,25 +37,39 @@ using Pair128F32 = GemmCfg<2, 8, false, 128>;   // CTA pair, 256 x 128 tile, 8 s
 using Pair128F16 = GemmCfg<2, 8, true, 128>;
 using Single64F32 = GemmCfg<1, 8, false, 64>;   // one CTA, 128 x 64 tile, 8 stages
 using Single64F16 = GemmCfg<1, 8, true, 64>;
+// Swapped roles for small M: 128 columns of C x 16/32/64 rows of C per CTA.
+using Swap16F32 = GemmCfg<1, 11, false, 16, true>;
+using Swap16F16 = GemmCfg<1, 11, true, 16, true>;
+using Swap32F32 = GemmCfg<1, 10, false, 32, true>;
+using Swap32F16 = GemmCfg<1, 10, true, 32, true>;
+using Swap64F32 = GemmCfg<1, 8, false, 64, true>;
+using Swap64F16 = GemmCfg<1, 8, true, 64, true>;
 
 struct VariantInfo {
   const char* name;
   int ctas;            // CTAs per tile (cluster size)
-  int tile_m, tile_n;  // output tile owned by one CTA or CTA pair
+  int tile_m, tile_n;  // output tile (rows x columns of C) owned by one CTA or CTA pair
   int box_a_rows;      // rows of A each CTA loads per stage
   int box_b_rows;      // rows of B each CTA loads per stage
+  bool swap;           // MMA roles swapped: the kernel's tiles run over (N, M)
 };
 
 constexpr int kVariantPair = 0;
 constexpr int kVariantSingle = 1;
 constexpr int kVariantPair128 = 2;
 constexpr int kVariantSingle64 = 3;
-constexpr int kNumVariants = 4;
+constexpr int kVariantSwap16 = 4;
+constexpr int kVariantSwap32 = 5;
+constexpr int kVariantSwap64 = 6;
+constexpr int kNumVariants = 7;
 constexpr VariantInfo kVariants[kNumVariants] = {
-    {"tc_pair_256x256_s6", 2, 256, 256, 128, 128},
-    {"tc_single_128x256_s4", 1, 128, 256, 128, 256},
-    {"tc_pair_256x128_s8", 2, 256, 128, 128, 64},
-    {"tc_single_128x64_s8", 1, 128, 64, 128, 64},
+    {"tc_pair_256x256_s6", 2, 256, 256, 128, 128, false},
+    {"tc_single_128x256_s4", 1, 128, 256, 128, 256, false},
+    {"tc_pair_256x128_s8", 2, 256, 128, 128, 64, false},
+    {"tc_single_128x64_s8", 1, 128, 64, 128, 64, false},
+    {"tc_swap_16x128_s11", 1, 16, 128, 16, 128, true},
+    {"tc_swap_32x128_s10", 1, 32, 128, 32, 128, true},
+    {"tc_swap_64x128_s8", 1, 64, 128, 64, 128, true},
 };
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s for any single wait
@@ -201,8 +216,18 @@ struct Schedule {
 // before its whole tiles), if the estimate (in k-block times per unit) says
 // it saves enough.  The testing mode 2 forces the share on any shape
 // (all tiles when T < 2U).
+// Automatic choice: swapped roles when C has few rows (the tile then wastes
+// no MMA rows on padding and the work is spread over all SMs), else the
+// CTA-pair kernel.
+int auto_variant(int64_t M) {
+  if (M <= 16) return kVariantSwap16;
+  if (M <= 32) return kVariantSwap32;
+  if (M <= 64) return kVariantSwap64;
+  return kVariantPair;
+}
+
 Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc) {
-  int v = p->forced_variant >= 0 ? p->forced_variant : kVariantPair;
+  int v = p->forced_variant >= 0 ? p->forced_variant : auto_variant(M);
   if (kVariants[v].ctas == 2 && p->max_pairs < 1) v = kVariantSingle;
   const VariantInfo& vi = kVariants[v];
   const int64_t T = tiles_of(vi, M, N);
@@ -218,9 +243,12 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
   // fix-ups then overlap those tiles' main loops.  With nothing after it, the
   // fix-ups end the kernel and cost more than the part-empty wave they save
   // (measured: 1024 x 8192 x 8192 at 119 us with the share, 88 us without).
+  // With swapped roles a partial tile is small (128 x 16..64 fp32), so the
+  // share is cheap even with no whole tiles after it: it is what spreads a
+  // few tall tiles over every SM.
   const bool allowed = acc == GEMM_ACC_F32 && p->sk_ws && p->sk_count && KB > 0 &&
                        p->schedule_mode != 1 &&
-                       ((T % U != 0 && T >= 2 * U) || p->schedule_mode == 2);
+                       ((T % U != 0 && (T >= 2 * U || vi.swap)) || p->schedule_mode == 2);
   if (allowed) {
     const int64_t sk_tiles = T >= U ? T % U + U : T;
     const int64_t dp = T - sk_tiles;
@@ -231,7 +259,7 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
     if (usk > U) usk = U;
     // At most about two contributors per tile: the last one reads the others'
     // partial tiles, and that read grows with their number.
-    if (p->schedule_mode != 2 && usk > 2 * sk_tiles) usk = 2 * sk_tiles;
+    if (p->schedule_mode != 2 && !vi.swap && usk > 2 * sk_tiles) usk = 2 * sk_tiles;
     const bool fits = static_cast<size_t>(sk_tiles * vi.ctas) <= p->sk_count_words;
     if (usk >= 2 && fits) {
       const double t_dp = static_cast<double>((T + U - 1) / U) * KB;
@@ -314,8 +342,17 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   args.M = static_cast<int32_t>(M);
   args.N = static_cast<int32_t>(N);
   args.K = static_cast<int32_t>(K);
-  args.tiles_m = static_cast<int32_t>((M + vi.tile_m - 1) / vi.tile_m);
-  args.tiles_n = static_cast<int32_t>((N + vi.tile_n - 1) / vi.tile_n);
+  if (vi.swap) {
+    // The kernel's "A" walks 128-row tiles of B, its "B" tiles of A's rows.
+    std::swap(ma, mb);
+    args.tiles_m = static_cast<int32_t>((N + vi.tile_n - 1) / vi.tile_n);
+    args.tiles_n = static_cast<int32_t>((M + vi.tile_m - 1) / vi.tile_m);
+  } else {
+    args.tiles_m = static_cast<int32_t>((M + vi.tile_m - 1) / vi.tile_m);
+    args.tiles_n = static_cast<int32_t>((N + vi.tile_n - 1) / vi.tile_n);
+  }
+  args.C = static_cast<uint16_t*>(C);
+  args.ldc = N;
   args.num_kb = static_cast<int32_t>((K + 63) / 64);
   args.num_tiles = args.tiles_m * args.tiles_n;
   args.group_m = kGroupM;
@@ -342,6 +379,18 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
     case kVariantSingle64:
       e = f32 ? launch_gemm<Single64F32>(ma, mb, mc, args, grid, stream)
               : launch_gemm<Single64F16>(ma, mb, mc, args, grid, stream);
+      break;
+    case kVariantSwap16:
+      e = f32 ? launch_gemm<Swap16F32>(ma, mb, mc, args, grid, stream)
+              : launch_gemm<Swap16F16>(ma, mb, mc, args, grid, stream);
+      break;
+    case kVariantSwap32:
+      e = f32 ? launch_gemm<Swap32F32>(ma, mb, mc, args, grid, stream)
+              : launch_gemm<Swap32F16>(ma, mb, mc, args, grid, stream);
+      break;
+    case kVariantSwap64:
+      e = f32 ? launch_gemm<Swap64F32>(ma, mb, mc, args, grid, stream)
+              : launch_gemm<Swap64F16>(ma, mb, mc, args, grid, stream);
       break;
     default:
       e = f32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, stream)
@@ -427,7 +476,10 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
   if (set_smem_attr<SingleF32>() != cudaSuccess || set_smem_attr<SingleF16>() != cudaSuccess ||
       set_smem_attr<PairF32>() != cudaSuccess || set_smem_attr<PairF16>() != cudaSuccess ||
       set_smem_attr<Pair128F32>() != cudaSuccess || set_smem_attr<Pair128F16>() != cudaSuccess ||
-      set_smem_attr<Single64F32>() != cudaSuccess || set_smem_attr<Single64F16>() != cudaSuccess) {
+      set_smem_attr<Single64F32>() != cudaSuccess || set_smem_attr<Single64F16>() != cudaSuccess ||
+      set_smem_attr<Swap16F32>() != cudaSuccess || set_smem_attr<Swap16F16>() != cudaSuccess ||
+      set_smem_attr<Swap32F32>() != cudaSuccess || set_smem_attr<Swap32F16>() != cudaSuccess ||
+      set_smem_attr<Swap64F32>() != cudaSuccess || set_smem_attr<Swap64F16>() != cudaSuccess) {
     delete p;
     return GEMM_ERR_CUDA;
   }
@@ -763,6 +815,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   args.sk_iters = 0;
   args.sk_ws = nullptr;
   args.sk_count = nullptr;
+  args.C = static_cast<uint16_t*>(C);
+  args.ldc = N;
   const int grid = args.num_tiles < d.num_sms ? args.num_tiles : d.num_sms;
   // The watchdog record must start at zero; the array keeps the last call's
   // contents, so clear it on the caller's stream before the launch.

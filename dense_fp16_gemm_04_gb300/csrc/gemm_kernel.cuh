@@ -70,6 +70,8 @@ struct GemmArgs {
   int64_t sk_iters;
   float* sk_ws;         // partial accumulators: [unit][2 slots][CTA of unit][128 x 256] fp32
   uint32_t* sk_count;   // per tail tile and CTA of the tile: contributions so far (self-resetting)
+  uint16_t* C;          // output (fp16 bits), row pitch ldc elements: the swapped-roles
+  int64_t ldc;          // epilogue stores directly
 };
 
 // One piece of work for a unit: k-blocks [kb0, kb1) of one output tile.
@@ -140,9 +142,12 @@ struct Sched {
 };
 
 // Tile configuration.  kCtas CTAs cooperate on one tile of kTileM x kBN.
-template <int kCtas_, int kStages_, bool kAccF16_, int kBN_ = 256>
+template <int kCtas_, int kStages_, bool kAccF16_, int kBN_ = 256, bool kSwap_ = false>
 struct GemmCfg {
   static constexpr int kCtas = kCtas_;
+  // Swapped roles (for small M): the MMA's "A" operand is a 128-row tile of B
+  // and its "B" operand a kBN-row tile of A, so D = tile of C^T.
+  static constexpr bool kSwap = kSwap_;
   static constexpr int kBM = 128;                 // rows of C per CTA
   static constexpr int kBN = kBN_;                // columns of C per tile
   static constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle row)
@@ -156,7 +161,7 @@ struct GemmCfg {
   static constexpr int kTxBytes = kStageBytes * kCtas;   // counted on the leader's barrier
   static constexpr int kEpiWarps = 4;
   static constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 fp16, 128B swizzle
-  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kEpiBytes = kSwap ? 0 : kEpiWarps * 2 * kEpiBufBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kStages * kABytes;
   static constexpr int kOffEpi = kStages * kStageBytes;
@@ -172,7 +177,9 @@ struct GemmCfg {
   static constexpr uint32_t kIdesc = ptx::idesc_f16(kTileM, kBN, !kAccF16);
 
   static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair");
-  static_assert(kBN == 64 || kBN == 128 || kBN == 256, "tile width 64, 128 or 256");
+  static_assert(kSwap ? (kCtas == 1 && (kBN == 16 || kBN == 32 || kBN == 64))
+                      : (kBN == 64 || kBN == 128 || kBN == 256),
+                "tile width: 64, 128 or 256; 16, 32 or 64 with swapped roles (one CTA)");
   static_assert(kBRows >= 8 && kBRows % 8 == 0, "B rows per CTA: whole 8-row swizzle atoms");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                 "TMEM is allocated in powers of two from 32 to 512 columns");
@@ -411,6 +418,122 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       else
         ptx::mma_commit(bar_mma_done);
       wait_bar<kPair>(bar_mma_done, 0u, w, kSiteMmaDone, -1, /*honor_abort=*/false);
+    }
+  } else if constexpr (Cfg::kSwap) {
+    // ---------------------------------------------- epilogue, swapped roles --
+    // The MMA computed a tile of C^T = B x A^T: TMEM lane = column n of C,
+    // TMEM column = row m of C.  Each thread owns one column n and stores its
+    // kBN values down it; for a fixed m the warp's 32 lanes write 32
+    // consecutive columns, 64 contiguous bytes per store.
+    const int q = warp & 3;  // this warp may touch TMEM lanes 32q .. 32q+31 only
+    const int row_in_cta = q * 32 + lane;
+    const uint32_t tempty_bar0 = bar_tempty(0);
+    volatile uint32_t* last_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffFlag);
+    auto partial = [&](int32_t u, int32_t slot) {
+      return args.sk_ws + static_cast<size_t>(u * 2 + slot) * static_cast<size_t>(Cfg::kPartialFloats);
+    };
+    Sched sched(args, unit, units);
+    WorkItem wi;
+    int32_t acc_iter = 0;
+    while (sched.next(wi)) {
+      int32_t mb, nb;
+      raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
+      const int buf = acc_iter & 1;
+      const uint32_t use_par = static_cast<uint32_t>((acc_iter >> 1) & 1);
+      ++acc_iter;
+      int ok = 1;
+      if (lane == 0) ok = wait_bar<false>(bar_tfull(buf), use_par, w, kSiteTmemFull, wi.tile) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ptx::named_barrier_and(1, 32 * Cfg::kEpiWarps, ok != 0)) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(buf * Cfg::kBN);
+      const int32_t n = mb * Cfg::kBM + row_in_cta;  // column of C
+      const int32_t m0 = nb * Cfg::kBN;              // first row of C in this tile
+      const bool split = !Cfg::kAccF16 && wi.splits > 1;
+      float acc[Cfg::kBN];
+      if (split) {
+        // Same protocol as the plain epilogue: park the fp32 partial, count,
+        // and the last contributor sums all partials in unit order.
+        float* own = partial(unit, sched.slot_of(unit, wi.sk_tile)) +
+                     static_cast<size_t>(row_in_cta) * 4;
+#pragma unroll
+        for (int g = 0; g < Cfg::kBN / 16; ++g) {
+          uint32_t v[16];
+          ptx::tmem_ld_32x32b_x16(t_row + g * 16, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            ptx::st_global_v4(own + static_cast<size_t>(g * 4 + j) * (Cfg::kBM * 4), v[4 * j],
+                              v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty_bar0 + 8u * buf);
+        __threadfence();
+        ptx::named_barrier_sync(1, 32 * Cfg::kEpiWarps);
+        if (threadIdx.x == 64) {
+          uint32_t* cnt = args.sk_count + static_cast<size_t>(wi.sk_tile);
+          const uint32_t before = atomicAdd(cnt, 1u);
+          const bool last = before == static_cast<uint32_t>(wi.splits - 1);
+          if (last) *cnt = 0u;
+          *last_flag = last ? 1u : 0u;
+        }
+        ptx::named_barrier_sync(1, 32 * Cfg::kEpiWarps);
+        if (*last_flag == 0u) continue;
+        __threadfence();
+#pragma unroll
+        for (int i = 0; i < Cfg::kBN; ++i) acc[i] = 0.0f;
+        for (int32_t j = 0; j < wi.splits; ++j) {
+          const int32_t u = wi.first_unit + j;
+          const float* src = partial(u, sched.slot_of(u, wi.sk_tile)) +
+                             static_cast<size_t>(row_in_cta) * 4;
+#pragma unroll
+          for (int g4 = 0; g4 < Cfg::kBN / 4; ++g4) {
+            const float4 v = ptx::ld_global_cg_v4(src + static_cast<size_t>(g4) * (Cfg::kBM * 4));
+            acc[4 * g4] += v.x;
+            acc[4 * g4 + 1] += v.y;
+            acc[4 * g4 + 2] += v.z;
+            acc[4 * g4 + 3] += v.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < Cfg::kBN / 16; ++g) {
+          if constexpr (Cfg::kAccF16) {
+            uint32_t v[8];
+            ptx::tmem_ld_32x32b_x8_pack16(t_row + g * 16, v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const __half2 h = *reinterpret_cast<const __half2*>(&v[i]);
+              acc[g * 16 + 2 * i] = __low2float(h);
+              acc[g * 16 + 2 * i + 1] = __high2float(h);
+            }
+          } else {
+            uint32_t v[16];
+            ptx::tmem_ld_32x32b_x16(t_row + g * 16, v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[g * 16 + i] = __uint_as_float(v[i]);
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty_bar0 + 8u * buf);
+      }
+      if (n < args.N) {
+        uint16_t* col = args.C + n;
+#pragma unroll
+        for (int i = 0; i < Cfg::kBN; ++i) {
+          const int32_t m = m0 + i;
+          if (m < args.M) {
+            const __half h = __float2half_rn(acc[i]);
+            ptx::st_global_b16(col + static_cast<size_t>(m) * args.ldc,
+                               *reinterpret_cast<const uint16_t*>(&h));
+          }
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue --

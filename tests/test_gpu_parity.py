@@ -8,7 +8,7 @@ import torch
 
 import gemm_workloads as wl
 import oracle
-from conftest import TOL, VARIANTS, assert_close, error_stats, read_golden, run_gpu, to_dev
+from conftest import TOL, VARIANTS, VARIANTS_WIDE, assert_close, error_stats, read_golden, run_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -122,7 +122,7 @@ def _sampled_parity(plan, w, acc):
     return st_r, st_c
 
 
-@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("variant", VARIANTS_WIDE)
 @pytest.mark.parametrize("name,acc", [
     ("gemm_4096", "f32"), ("gemm_8192", "f32"), ("gemm_8192", "f16"),
     ("gemm_ragged_3000x5000x4104", "f32"), ("gemm_16384", "f32")])
@@ -134,7 +134,7 @@ def test_workload_sampled(plans, variant, name, acc):
         assert st_r["max_abs"] <= pages["atol"] and st_c["max_abs"] <= pages["atol"]
 
 
-@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("variant", VARIANTS_WIDE)
 def test_16384_all_ones_closed_form(plans, variant):
     M = N = K = 16384
     a = torch.ones((M, K), dtype=torch.float16, device="cuda")
@@ -155,3 +155,26 @@ def test_8192_fp16_accumulate_error_distribution(plan):
     _, pages = read_golden("pages_fp16_acc_error.txt")
     print(f"fp16-acc K=8192: ours {st}  pages mean {pages['mean']} p99 {pages['p99']} max {pages['max']}")
     assert st["max_abs"] <= pages["atol"]
+
+
+# ------------------------------------------------------------ few rows of C --
+SKINNY = [(1, 8, 64), (1, 1032, 4104), (3, 520, 328), (16, 4096, 1024), (17, 264, 520),
+          (32, 2056, 2048), (48, 1000, 776), (64, 8192, 512), (65, 264, 136)]
+
+
+@pytest.mark.parametrize("shape", SKINNY, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("acc", ["f32", "f16"])
+def test_skinny_auto(plan, shape, acc):
+    M, N, K = shape
+    a, b = wl.draw(M, N, K, seed=M * 5 + N + K)
+    assert_close(run_gpu(plan, a, b, acc), oracle.gemm_f64(a, b), acc,
+                 f"{shape} {acc} {plan.describe(M, N, K, acc)}")
+
+
+@pytest.mark.parametrize("variant", ["tc_swap_16x128_s11", "tc_swap_32x128_s10", "tc_swap_64x128_s8"])
+def test_skinny_8192(plans, variant):
+    """A decode-like shape (few rows, wide and deep) on every swapped-roles
+    variant, checked on all rows against the oracle."""
+    M, N, K = 16, 8192, 8192
+    a, b = wl.draw(M, N, K, seed=88)
+    assert_close(run_gpu(plans[variant], a, b), oracle.gemm_f64(a, b), "f32", variant)

@@ -29,13 +29,17 @@ def test_stuck_wait_reports_timeout_and_context_survives(variant):
     a, b = wl.draw(M, N, K, seed=51)
     ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
 
+    # Unit 0's first piece of work: the first shared tile when the schedule
+    # has a stream-K share (it runs first), else tile 0.
+    d = p.describe(M, N, K)
+    first_tile = d["dp_tiles"] if d["sk_units"] > 0 else 0
     p.set_watchdog(timeout_ns=TIMEOUT_NS, skip_k_block=0)
     c = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
     p.run(ta, tb, c)                          # the launch itself succeeds
     status = p.check_error_status()
     assert status == 5, g.status_string(status)
     code, site, cta, tile = p.last_error_detail()
-    assert code == 5 and site in STUCK_SITES and cta in (0, 1) and tile == 0
+    assert code == 5 and site in STUCK_SITES and cta in (0, 1) and tile == first_tile
     assert p.check_error_status() == 0        # the record was cleared
 
     # Back to normal: same plan, same context.
