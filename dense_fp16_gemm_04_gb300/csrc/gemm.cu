@@ -216,13 +216,16 @@ struct Schedule {
 // before its whole tiles), if the estimate (in k-block times per unit) says
 // it saves enough.  The testing mode 2 forces the share on any shape
 // (all tiles when T < 2U).
-// Automatic choice: swapped roles when C has few rows (the tile then wastes
-// no MMA rows on padding and the work is spread over all SMs), else the
-// CTA-pair kernel.
+// Automatic choice, from measurements on GB300 (N = K = 8192 unless noted):
+// swapped roles when C has at most 64 rows (the tile then wastes no MMA rows
+// on padding and the work is spread over all SMs: 16 rows 32 us vs 42 us);
+// one CTA with 128 x 64 tiles up to 128 rows (more, narrower tiles: 41 us vs
+// 46 us for the pair); the CTA-pair kernel above that.
 int auto_variant(int64_t M) {
   if (M <= 16) return kVariantSwap16;
   if (M <= 32) return kVariantSwap32;
   if (M <= 64) return kVariantSwap64;
+  if (M <= 128) return kVariantSingle64;
   return kVariantPair;
 }
 
