@@ -25,12 +25,15 @@ from . import _build
 
 __all__ = [
     "build", "load", "Plan", "GemmError", "gemm", "gemm_host", "default_plan",
-    "ACC_F32", "ACC_F16", "status_string", "variant_names", "LIB_PATH",
+    "ACC_F32", "ACC_F16", "K_CONTIGUOUS", "MN_CONTIGUOUS", "status_string", "variant_names",
+    "LIB_PATH",
 ]
 
 LIB_PATH = _build.LIB_PATH
 ACC_F32 = 0
 ACC_F16 = 1
+K_CONTIGUOUS = 0    # A stored [M, K], B stored [N, K]
+MN_CONTIGUOUS = 1   # A stored [K, M], B stored [K, N]
 _ACC = {"f32": ACC_F32, "fp32": ACC_F32, "float32": ACC_F32, ACC_F32: ACC_F32,
         "f16": ACC_F16, "fp16": ACC_F16, "float16": ACC_F16, ACC_F16: ACC_F16}
 
@@ -74,6 +77,8 @@ def load():
             "gemm_plan_destroy": (st, [vp]),
             "gemm_run": (st, [vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]),
             "gemm_run_host": (st, [vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]),
+            "gemm_run_ex": (st, [vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, i64, i64, i64,
+                                 ctypes.c_int, vp]),
             "gemm_plan_check_error": (st, [vp]),
             "gemm_plan_last_error_detail": (st, [vp, ctypes.POINTER(ctypes.c_uint32)]),
             "gemm_plan_set_watchdog": (st, [vp, u64, i32]),
@@ -162,16 +167,26 @@ class Plan:
         _check(self._lib.gemm_run_host(self._h, a_ptr, b_ptr, c_ptr, M, N, K, _acc(acc), stream),
                "gemm_run_host")
 
+    def run_ex_ptr(self, a_ptr: int, layout_a: int, b_ptr: int, layout_b: int, c_ptr: int,
+                   M: int, N: int, K: int, acc="f32", stream: int = 0) -> None:
+        _check(self._lib.gemm_run_ex(self._h, a_ptr, int(layout_a), b_ptr, int(layout_b), c_ptr,
+                                     M, N, K, _acc(acc), stream), "gemm_run_ex")
+
     def status_run(self, a_ptr, b_ptr, c_ptr, M, N, K, acc=0, stream=0) -> int:
         """gemm_run's raw status code (no exception)."""
         return self._lib.gemm_run(self._h, a_ptr, b_ptr, c_ptr, M, N, K, int(acc), stream)
 
     # -- torch tensor interface ------------------------------------------------
     def run(self, a, b, c, acc="f32", stream=None) -> None:
-        """C = A @ B.T on CUDA tensors (fp16, contiguous, A [M,K], B [N,K], C [M,N])."""
-        M, N, K = _check_tensors(a, b, c)
-        self.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, acc,
-                     _stream_handle(stream))
+        """C = A @ B.T on CUDA tensors: fp16, A [M,K], B [N,K], C [M,N] contiguous.
+        A and B may each be contiguous or the transpose of a contiguous tensor
+        (A = x.t() with x [K,M]; B = w.t() with w [K,N], i.e. C = A @ w)."""
+        M, N, K, la, lb = _check_tensors(a, b, c)
+        sh = _stream_handle(stream)
+        if la == K_CONTIGUOUS and lb == K_CONTIGUOUS:
+            self.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, acc, sh)
+        else:
+            self.run_ex_ptr(a.data_ptr(), la, b.data_ptr(), lb, c.data_ptr(), M, N, K, acc, sh)
 
     def run_host(self, a, b, c, acc="f32", stream=None) -> None:
         """Same on CPU tensors/arrays (pinned for full copy speed); synchronous."""
@@ -228,6 +243,16 @@ class Plan:
         return int(self._lib.gemm_plan_launch_count(self._h))
 
 
+def _layout(t, name):
+    """K_CONTIGUOUS for a contiguous [rows, K] tensor, MN_CONTIGUOUS for the
+    transpose of a contiguous [K, rows] tensor."""
+    if t.is_contiguous():
+        return K_CONTIGUOUS
+    if t.t().is_contiguous():
+        return MN_CONTIGUOUS
+    raise ValueError(f"{name} must be contiguous or the transpose of a contiguous tensor")
+
+
 def _check_tensors(a, b, c):
     import torch
     for name, t in (("A", a), ("B", b), ("C", c)):
@@ -235,14 +260,16 @@ def _check_tensors(a, b, c):
             raise TypeError(f"{name} must be float16, got {t.dtype}")
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
-        if t.dim() != 2 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 2-D tensor")
+        if t.dim() != 2:
+            raise ValueError(f"{name} must be a 2-D tensor")
+    if not c.is_contiguous():
+        raise ValueError("C must be contiguous")
     M, K = a.shape
     N = b.shape[0]
     if b.shape[1] != K or tuple(c.shape) != (M, N):
         raise ValueError(f"want A [M,K], B [N,K], C [M,N]; got {tuple(a.shape)}, "
                          f"{tuple(b.shape)}, {tuple(c.shape)}")
-    return M, N, K
+    return M, N, K, _layout(a, "A"), _layout(b, "B")
 
 
 def _host_ptr(x) -> int:

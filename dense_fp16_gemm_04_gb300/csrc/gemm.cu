@@ -229,8 +229,12 @@ int auto_variant(int64_t M) {
   return kVariantPair;
 }
 
-Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc) {
+// `mn`: an operand is stored M- or N-contiguous (the swapped-roles variants
+// take K-contiguous operands only).
+Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
+                       bool mn = false) {
   int v = p->forced_variant >= 0 ? p->forced_variant : auto_variant(M);
+  if (mn && kVariants[v].swap) v = M <= 128 ? kVariantSingle64 : kVariantPair;
   if (kVariants[v].ctas == 2 && p->max_pairs < 1) v = kVariantSingle;
   const VariantInfo& vi = kVariants[v];
   const int64_t T = tiles_of(vi, M, N);
@@ -324,7 +328,8 @@ int max_active_pairs() {
 }
 
 gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, int64_t M,
-                         int64_t N, int64_t K, gemm_acc_t acc, cudaStream_t stream) {
+                         int64_t N, int64_t K, gemm_acc_t acc, cudaStream_t stream,
+                         int la = GEMM_K_CONTIGUOUS, int lb = GEMM_K_CONTIGUOUS) {
   if (K == 0) {
     const int64_t n16 = M * N * 2 / 16;
     const int64_t blocks = (n16 + 255) / 256;
@@ -333,13 +338,19 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
     ++p->launches;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
-  const Schedule sch = make_schedule(p, M, N, K, acc);
+  const bool a_mn = la == GEMM_MN_CONTIGUOUS, b_mn = lb == GEMM_MN_CONTIGUOUS;
+  const Schedule sch = make_schedule(p, M, N, K, acc, a_mn || b_mn);
   const int grid = sch.grid;
   const VariantInfo& vi = kVariants[sch.variant];
+  if (vi.swap && (a_mn || b_mn)) return GEMM_ERR_INVALID_ARG;  // forced swapped variant
+  // K-contiguous operands: boxes of 64 K-elements x the tile's rows.
+  // M/N-contiguous operands (stored [K, M] / [K, N]): boxes of 64 x 64.
   CUtensorMap ma, mb, mc;
-  if (!get_map(p, &ma, A, M, K, vi.box_a_rows, 64) || !get_map(p, &mb, B, N, K, vi.box_b_rows, 64) ||
-      !get_map(p, &mc, C, M, N, 32, 64))
-    return GEMM_ERR_CUDA;
+  const bool maps_ok =
+      (a_mn ? get_map(p, &ma, A, K, M, 64, 64) : get_map(p, &ma, A, M, K, vi.box_a_rows, 64)) &&
+      (b_mn ? get_map(p, &mb, B, K, N, 64, 64) : get_map(p, &mb, B, N, K, vi.box_b_rows, 64)) &&
+      get_map(p, &mc, C, M, N, 32, 64);
+  if (!maps_ok) return GEMM_ERR_CUDA;
 
   GemmArgs args;
   args.M = static_cast<int32_t>(M);
@@ -356,6 +367,8 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   }
   args.C = static_cast<uint16_t*>(C);
   args.ldc = N;
+  args.a_mn = a_mn ? 1 : 0;
+  args.b_mn = b_mn ? 1 : 0;
   args.num_kb = static_cast<int32_t>((K + 63) / 64);
   args.num_tiles = args.tiles_m * args.tiles_n;
   args.group_m = kGroupM;
@@ -602,6 +615,37 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, int
   return run_device(p, A, B, C, M, N, K, acc, static_cast<cudaStream_t>(stream));
 }
 
+gemm_status_t gemm_run_ex(gemm_plan_t p, const void* A, gemm_layout_t layout_a, const void* B,
+                          gemm_layout_t layout_b, void* C, int64_t M, int64_t N, int64_t K,
+                          gemm_acc_t acc, void* stream) {
+  if (!p) return GEMM_ERR_INVALID_ARG;
+  const bool la_ok = layout_a == GEMM_K_CONTIGUOUS || layout_a == GEMM_MN_CONTIGUOUS;
+  const bool lb_ok = layout_b == GEMM_K_CONTIGUOUS || layout_b == GEMM_MN_CONTIGUOUS;
+  if (!la_ok || !lb_ok) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+    return GEMM_ERR_INVALID_ARG;
+  if (acc != GEMM_ACC_F32 && acc != GEMM_ACC_F16) return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  // Every stored row must start on a 16-byte boundary: the contiguous
+  // dimension of each operand, and N for C, is a multiple of 8.
+  if (N % 8 != 0) return GEMM_ERR_ALIGNMENT;
+  if ((layout_a == GEMM_K_CONTIGUOUS || layout_b == GEMM_K_CONTIGUOUS) && K % 8 != 0)
+    return GEMM_ERR_ALIGNMENT;
+  if (layout_a == GEMM_MN_CONTIGUOUS && M % 8 != 0) return GEMM_ERR_ALIGNMENT;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(C) & 15) ||
+      (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))))
+    return GEMM_ERR_ALIGNMENT;
+  const size_t bytesC = static_cast<size_t>(M) * N * 2;
+  if (K > 0 && (overlaps(C, bytesC, A, static_cast<size_t>(M) * K * 2) ||
+                overlaps(C, bytesC, B, static_cast<size_t>(N) * K * 2)))
+    return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  return run_device(p, A, B, C, M, N, K, acc, static_cast<cudaStream_t>(stream), layout_a,
+                    layout_b);
+}
+
 gemm_status_t gemm_plan_check_error(gemm_plan_t p) {
   if (!p) return GEMM_ERR_INVALID_ARG;
   DeviceGuard g(p->device);
@@ -820,6 +864,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   args.sk_count = nullptr;
   args.C = static_cast<uint16_t*>(C);
   args.ldc = N;
+  args.a_mn = 0;
+  args.b_mn = 0;
   const int grid = args.num_tiles < d.num_sms ? args.num_tiles : d.num_sms;
   // The watchdog record must start at zero; the array keeps the last call's
   // contents, so clear it on the caller's stream before the launch.

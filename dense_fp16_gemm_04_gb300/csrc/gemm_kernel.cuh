@@ -60,6 +60,9 @@ struct GemmArgs {
   uint32_t* err;        // device watchdog record, 4 words
   uint64_t timeout_ns;  // longest allowed single wait
   int32_t skip_kb;      // fault injection, -1 = off
+  // Operand layouts: 0 = K contiguous (A [M,K], B [N,K]); 1 = M (resp. N)
+  // contiguous (A stored [K,M], B stored [K,N]); loaded as 64 x 64 boxes.
+  int32_t a_mn, b_mn;
   // Schedule: tiles [0, dp_tiles) are dealt out whole, round robin over the
   // units (CTAs or CTA pairs).  The remaining tiles form the stream-K tail:
   // their sk_iters = (num_tiles - dp_tiles) * num_kb k-blocks are cut into
@@ -331,12 +334,40 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               // leader declares them all.
               const uint32_t full_leader = ptx::mapa(bar_full(stage), 0);
               if (rank == 0) ptx::mbar_arrive_expect_tx(bar_full(stage), Cfg::kTxBytes);
-              ptx::tma_load_2d_pair(sA(stage), &tmA, full_leader, kb * Cfg::kBK, a_row);
-              ptx::tma_load_2d_pair(sB(stage), &tmB, full_leader, kb * Cfg::kBK, b_row);
+              if (args.a_mn) {
+#pragma unroll
+                for (int g = 0; g < Cfg::kBM / 64; ++g)
+                  ptx::tma_load_2d_pair(sA(stage) + g * 8192, &tmA, full_leader, a_row + 64 * g,
+                                        kb * Cfg::kBK);
+              } else {
+                ptx::tma_load_2d_pair(sA(stage), &tmA, full_leader, kb * Cfg::kBK, a_row);
+              }
+              if (args.b_mn) {
+#pragma unroll
+                for (int g = 0; g < Cfg::kBRows / 64; ++g)
+                  ptx::tma_load_2d_pair(sB(stage) + g * 8192, &tmB, full_leader, b_row + 64 * g,
+                                        kb * Cfg::kBK);
+              } else {
+                ptx::tma_load_2d_pair(sB(stage), &tmB, full_leader, kb * Cfg::kBK, b_row);
+              }
             } else {
               ptx::mbar_arrive_expect_tx(bar_full(stage), Cfg::kTxBytes);
-              ptx::tma_load_2d(sA(stage), &tmA, bar_full(stage), kb * Cfg::kBK, a_row);
-              ptx::tma_load_2d(sB(stage), &tmB, bar_full(stage), kb * Cfg::kBK, b_row);
+              if (args.a_mn) {
+#pragma unroll
+                for (int g = 0; g < Cfg::kBM / 64; ++g)
+                  ptx::tma_load_2d(sA(stage) + g * 8192, &tmA, bar_full(stage), a_row + 64 * g,
+                                   kb * Cfg::kBK);
+              } else {
+                ptx::tma_load_2d(sA(stage), &tmA, bar_full(stage), kb * Cfg::kBK, a_row);
+              }
+              if (args.b_mn) {
+#pragma unroll
+                for (int g = 0; g < Cfg::kBRows / 64; ++g)
+                  ptx::tma_load_2d(sB(stage) + g * 8192, &tmB, bar_full(stage), b_row + 64 * g,
+                                   kb * Cfg::kBK);
+              } else {
+                ptx::tma_load_2d(sB(stage), &tmB, bar_full(stage), kb * Cfg::kBK, b_row);
+              }
             }
           }
           ++fills;
@@ -365,6 +396,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ------------------------------------------------------- MMA issuer --
+      const uint32_t idesc = Cfg::kIdesc | (args.a_mn ? ptx::kIdescAMnMajor : 0u) |
+                             (args.b_mn ? ptx::kIdescBMnMajor : 0u);
+      const uint64_t a_kstep = args.a_mn ? 128u : 2u;
+      const uint64_t b_kstep = args.b_mn ? 128u : 2u;
       Sched sched(args, unit, units);
       WorkItem wi;
       int stage = 0;
@@ -386,13 +421,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint64_t a_desc = ptx::sw128_kmajor_desc(sA(stage));
-          const uint64_t b_desc = ptx::sw128_kmajor_desc(sB(stage));
+          const uint64_t a_desc = args.a_mn ? ptx::sw128_mnmajor_desc(sA(stage))
+                                            : ptx::sw128_kmajor_desc(sA(stage));
+          const uint64_t b_desc = args.b_mn ? ptx::sw128_mnmajor_desc(sB(stage))
+                                            : ptx::sw128_kmajor_desc(sB(stage));
 #pragma unroll
           for (int k = 0; k < Cfg::kBK / 16; ++k) {
-            // +32 bytes along K per 16-element step, inside the swizzled row;
-            // the first step of the item overwrites the accumulator.
-            ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+            // One 16-deep K step: +32 bytes inside the swizzled row (K-major)
+            // or +16 K-rows = 2048 bytes (MN-major); descriptors count in 16 B.
+            // The first step of the item overwrites the accumulator.
+            ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + a_kstep * k, b_desc + b_kstep * k, idesc,
                                      (kb != wi.kb0 || k != 0) ? 1u : 0u);
           }
           if constexpr (kPair)

@@ -375,10 +375,28 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_byte_addr) {
   return d;
 }
 
-// Instruction descriptor for tcgen05.mma kind::f16 with fp16 A and B, both
-// K-major: D format (bits 4-5: 0 = f16, 1 = f32), A/B format 0 = f16 (bits
-// 7-9, 10-12), no negation, no transpose (bits 15, 16), N >> 3 (bits 17-22),
-// M >> 4 (bits 24-28).
+// Shared-memory matrix descriptor for an MN-major operand tile written by TMA
+// as boxes of 64 MN-elements (128 B) x 64 K-rows with 128-byte swizzle: each
+// K-row of a box is 128 contiguous MN bytes, 8-row swizzle atoms of 1024 B
+// stack along K (stride byte offset 1024 B), and successive 64-element groups
+// along M/N are one box apart (leading byte offset = box bytes, 8 KB).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_byte_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_byte_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(8192u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+// Instruction descriptor for tcgen05.mma kind::f16 with fp16 A and B: D
+// format (bits 4-5: 0 = f16, 1 = f32), A/B format 0 = f16 (bits 7-9, 10-12),
+// no negation, A/B major-ness (bits 15, 16: 0 = K-major, 1 = MN-major; OR'ed
+// in at run time), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+constexpr uint32_t kIdescAMnMajor = 1u << 15;
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
+
 __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool d_f32) {
   return (static_cast<uint32_t>(d_f32 ? 1 : 0) << 4) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);

@@ -53,6 +53,21 @@ typedef enum {
     GEMM_ACC_F16 = 1  /* native fp16 accumulate, fp16 output */
 } gemm_acc_t;
 
+/* Storage of an operand (gemm_run_ex).  Logically A is M x K and B is N x K
+ * whatever the storage:
+ *   GEMM_K_CONTIGUOUS : A stored [M, K], B stored [N, K] (rows along K; the
+ *                       layout of gemm_run)
+ *   GEMM_MN_CONTIGUOUS: A stored [K, M] (A(m,k) at A[k*M + m]), B stored
+ *                       [K, N] (B(n,k) at B[k*N + n]); with B so stored the
+ *                       call computes the usual row-major C = A x B.
+ * The tensor cores read both forms directly (tilus "A Minimal Hopper
+ * Matmul", "Block Tiling", note "Data layout: K-major": operands may be
+ * K-contiguous or MN-contiguous). */
+typedef enum {
+    GEMM_K_CONTIGUOUS = 0,
+    GEMM_MN_CONTIGUOUS = 1
+} gemm_layout_t;
+
 typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = 1,        /* null plan/pointer, negative or oversized dim, bad enum, C overlaps A or B */
@@ -90,6 +105,15 @@ GEMM_API gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 GEMM_API gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, void* C,
                        int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
                        void* stream);
+
+/* gemm_run with a choice of storage for each operand (see gemm_layout_t).
+ * Alignment rules: N % 8 == 0 always (rows of C); K % 8 == 0 if either
+ * operand is K-contiguous; M % 8 == 0 if A is M-contiguous; pointers 16-byte
+ * aligned.  Otherwise as gemm_run (asynchronous, allocates nothing). */
+GEMM_API gemm_status_t gemm_run_ex(gemm_plan_t plan, const void* A, gemm_layout_t layout_a,
+                                   const void* B, gemm_layout_t layout_b, void* C,
+                                   int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
+                                   void* stream);
 
 /* Same product on HOST buffers, synchronous: copies B and then row chunks of
  * A to device staging buffers owned by the plan (grown with cudaMalloc on
