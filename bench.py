@@ -45,6 +45,10 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="gemm_8192", choices=list(wl.WORKLOADS))
+    p.add_argument("--shape", default=None,
+                   help="MxNxK: time this shape instead (seeded N(0,1)*K^-1/4 inputs, seed 0)")
+    p.add_argument("--layout", default="kk", choices=["kk", "kn", "mk", "mn"],
+                   help="storage of A and B: k = K-contiguous, m/n = M/N-contiguous")
     p.add_argument("--acc", default="f32", choices=["f32", "f16"])
     p.add_argument("--variant", default=None, help="force a kernel variant by name")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -185,11 +189,19 @@ def cpu_oracle_rate(w, rows_req=0, steps=1, a=None, b=None):
     return rate, used, sample, times
 
 
+def resolve_workload(args):
+    """The named workload, or an ad-hoc one from --shape."""
+    if args.shape:
+        M, N, K = (int(v) for v in args.shape.lower().split("x"))
+        return wl.Workload(f"shape_{M}x{N}x{K}", M, N, K, 0, "normal", ("f32", "f16"))
+    return wl.WORKLOADS[args.workload]
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    w = wl.WORKLOADS[args.workload]
+    w = resolve_workload(args)
     a, b = wl.inputs_for(w)
     # each step: a bounded row sample sized so warmup+steps end in a few minutes
     budget_s = 150.0
@@ -237,17 +249,22 @@ def run_ours(args):
     plan = g.Plan(local)
     if args.variant:
         plan.set_variant(args.variant)
-    w = wl.WORKLOADS[args.workload]
+    w = resolve_workload(args)
     a_np, b_np = wl.inputs_for(w)
-    a = torch.from_numpy(a_np).to(dev)
-    b = torch.from_numpy(b_np).to(dev)
+    la = g.MN_CONTIGUOUS if args.layout[0] == "m" else g.K_CONTIGUOUS
+    lb = g.MN_CONTIGUOUS if args.layout[1] == "n" else g.K_CONTIGUOUS
+    a = torch.from_numpy(a_np if la == g.K_CONTIGUOUS else np.ascontiguousarray(a_np.T)).to(dev)
+    b = torch.from_numpy(b_np if lb == g.K_CONTIGUOUS else np.ascontiguousarray(b_np.T)).to(dev)
     c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     aptr, bptr, cptr = a.data_ptr(), b.data_ptr(), c.data_ptr()
 
     def step():
-        plan.run_ptr(aptr, bptr, cptr, w.M, w.N, w.K, args.acc, sh)
+        if la == g.K_CONTIGUOUS and lb == g.K_CONTIGUOUS:
+            plan.run_ptr(aptr, bptr, cptr, w.M, w.N, w.K, args.acc, sh)
+        else:
+            plan.run_ex_ptr(aptr, la, bptr, lb, cptr, w.M, w.N, w.K, args.acc, sh)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -289,7 +306,7 @@ def run_ours(args):
 
     # ------------------------------------------------- end to end, host API --
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.layout == "kk":
         ha = torch.from_numpy(a_np).pin_memory()
         hb = torch.from_numpy(b_np).pin_memory()
         hc = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
@@ -312,7 +329,8 @@ def run_ours(args):
         rate, used, sample, _ = cpu_oracle_rate(w, args.cpu_rows, steps=1, a=a_np, b=b_np)
         cpu = {"value": rate, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample}
 
-    traffic = _recorded_traffic(w.name, args.acc, plan.pick_variant(w.M, w.N, w.K, args.acc)[0])
+    traffic = (_recorded_traffic(w.name, args.acc, plan.pick_variant(w.M, w.N, w.K, args.acc)[0])
+               if args.layout == "kk" else None)
     variant, grid = plan.pick_variant(w.M, w.N, w.K, args.acc)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -320,7 +338,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.describe()}", "M": w.M, "N": w.N, "K": w.K,
-                   "acc": args.acc, "variant": variant, "grid_ctas": grid,
+                   "acc": args.acc, "layout": args.layout, "variant": variant, "grid_ctas": grid,
                    "l2": "inputs larger than L2 (A+B = %d MB vs 129 MB L2), no flush"
                          % ((a_np.nbytes + b_np.nbytes) >> 20),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

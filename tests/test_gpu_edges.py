@@ -150,3 +150,32 @@ def test_variant_choice_and_launch_count(plan):
     n0 = plan.launch_count
     run_gpu(plan, *wl.draw(128, 128, 64, seed=36))
     assert plan.launch_count == n0 + 1
+
+
+def test_cuda_graph_capture_and_replay():
+    """gemm_run only enqueues one kernel on the caller's stream (the tensor
+    maps travel as kernel parameters and the stream-K counters reset
+    themselves), so a captured call replays correctly, stream-K share
+    included."""
+    M, N, K = 4096, 4096, 1024          # 256 pair tiles: whole tiles + a stream-K share
+    a, b = wl.draw(M, N, K, seed=37)
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    c = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    p = g.Plan(0)
+    assert p.describe(M, N, K)["sk_units"] > 0
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        p.run(ta, tb, c)                 # first call outside the capture
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        p.run(ta, tb, c)
+    rows = wl.sample_indices(M, 48, 38)
+    ref = oracle.gemm_rows_f64(a, b, rows)
+    for _ in range(3):
+        c.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_close(c.cpu().numpy()[rows], ref, "f32", "graph replay")
+    p.check_error()
+    p.close()
