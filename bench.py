@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--workload", default="gemm_8192", choices=list(wl.WORKLOADS))
     p.add_argument("--shape", default=None,
                    help="MxNxK: time this shape instead (seeded N(0,1)*K^-1/4 inputs, seed 0)")
+    p.add_argument("--split", default="replicas", choices=["replicas", "m"],
+                   help="N > 1: every rank runs the whole workload (replicas, weak scaling) or "
+                        "its share of C's rows (m, strong scaling)")
     p.add_argument("--layout", default="kk", choices=["kk", "kn", "mk", "mn"],
                    help="storage of A and B: k = K-contiguous, m/n = M/N-contiguous")
     p.add_argument("--acc", default="f32", choices=["f32", "f16"])
@@ -249,8 +252,15 @@ def run_ours(args):
     plan = g.Plan(local)
     if args.variant:
         plan.set_variant(args.variant)
-    w = resolve_workload(args)
-    a_np, b_np = wl.inputs_for(w)
+    w_full = resolve_workload(args)
+    w = w_full
+    a_np, b_np = wl.inputs_for(w_full)
+    if world > 1 and args.split == "m":
+        # This rank's rows of A and C; B whole.  No exchange inside the product.
+        row0, rows = g.shard_rows(w_full.M, world, rank)
+        a_np = np.ascontiguousarray(a_np[row0:row0 + rows])
+        w = wl.Workload(f"{w_full.name}_rows{row0}+{rows}", rows, w_full.N, w_full.K, w_full.seed,
+                        w_full.dist, w_full.accs)
     la = g.MN_CONTIGUOUS if args.layout[0] == "m" else g.K_CONTIGUOUS
     lb = g.MN_CONTIGUOUS if args.layout[1] == "n" else g.K_CONTIGUOUS
     a = torch.from_numpy(a_np if la == g.K_CONTIGUOUS else np.ascontiguousarray(a_np.T)).to(dev)
@@ -298,7 +308,10 @@ def run_ours(args):
     clocks = sampler.summary()
 
     flops = float(w.flops)
-    value = aggregate_tflops(world, args.steps, flops, total_ms * 1e-3)
+    strong = world > 1 and args.split == "m"
+    # replicas: every rank did its own full problem; m: the ranks together did one.
+    value = (aggregate_tflops(1, args.steps, float(w_full.flops), total_ms * 1e-3) if strong
+             else aggregate_tflops(world, args.steps, flops, total_ms * 1e-3))
     ms_per_step = total_ms / args.steps
     peaks = measured_peaks()
     kernel_ms = statistics.mean(per_launch_ms)
@@ -319,7 +332,8 @@ def run_ours(args):
         for _ in range(e_steps):
             plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)
         dt = reduce_max(time.perf_counter() - t0, world, dev)
-        e2e = {"value": aggregate_tflops(world, e_steps, flops, dt), "unit": UNIT,
+        e2e = {"value": (aggregate_tflops(1, e_steps, float(w_full.flops), dt) if strong
+                         else aggregate_tflops(world, e_steps, flops, dt)), "unit": UNIT,
                "h2d_bytes_per_step": int(a_np.nbytes + b_np.nbytes),
                "d2h_bytes_per_step": int(w.M * w.N * 2),
                "ms_per_step": dt / e_steps * 1e3, "steps": e_steps}
@@ -335,13 +349,14 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "higher_is_better": True, "scaling": "strong" if strong else "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.describe()}", "M": w.M, "N": w.N, "K": w.K,
+        "config": {"workload": f"{w_full.name}: {w_full.describe()}", "M": w_full.M, "N": w.N, "K": w.K,
                    "acc": args.acc, "layout": args.layout, "variant": variant, "grid_ctas": grid,
                    "l2": "inputs larger than L2 (A+B = %d MB vs 129 MB L2), no flush"
                          % ((a_np.nbytes + b_np.nbytes) >> 20),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": (f"M split x{world}" if strong else f"replicas x{world}")
+                                  if world > 1 else "single GPU"},
         "pct_of_peak": value / world / peaks["tflops"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["tflops"],

@@ -24,7 +24,7 @@ import threading
 from . import _build
 
 __all__ = [
-    "build", "load", "Plan", "GemmError", "gemm", "gemm_host", "default_plan",
+    "build", "load", "Plan", "GemmError", "gemm", "gemm_host", "default_plan", "shard_rows",
     "ACC_F32", "ACC_F16", "K_CONTIGUOUS", "MN_CONTIGUOUS", "status_string", "variant_names",
     "LIB_PATH",
 ]
@@ -321,3 +321,19 @@ def gemm_host(a, b, acc="f32", out=None, stream=None, plan: Plan | None = None):
                           pin_memory=bool(getattr(a, "is_pinned", lambda: False)()))
     (plan or default_plan()).run_host(a, b, out, acc=acc, stream=stream)
     return out
+
+
+def shard_rows(M: int, world: int, rank: int, align: int = 256):
+    """Rows [row0, row0 + rows) of C (and A) owned by `rank` of `world` when one
+    GEMM is split over GPUs by rows: each rank multiplies its rows of A by all
+    of B, with no exchange inside the product.  Shard starts are multiples of
+    `align` (a whole number of 256-row tiles) except where M itself ends, and
+    the shards cover [0, M) exactly once."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("need 0 <= rank < world")
+    tiles = -(-M // align)
+    t0 = tiles * rank // world
+    t1 = tiles * (rank + 1) // world
+    row0 = min(M, t0 * align)
+    row1 = min(M, t1 * align)
+    return row0, row1 - row0

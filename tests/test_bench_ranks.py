@@ -75,3 +75,46 @@ def test_reference_arm_prints_one_line_on_rank_0():
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_shard_rows_cover_every_row_once():
+    import dense_fp16_gemm_04_gb300 as g
+    for M in [1, 7, 255, 256, 257, 3000, 8192, 16384, 100000]:
+        for world in [1, 2, 3, 4, 8]:
+            covered = []
+            for rank in range(world):
+                row0, rows = g.shard_rows(M, world, rank)
+                assert rows >= 0 and (row0 % 256 == 0 or rows == 0 or row0 == M)
+                covered.extend(range(row0, row0 + rows))
+            assert covered == list(range(M)), (M, world)
+    with pytest.raises(ValueError):
+        g.shard_rows(10, 2, 2)
+
+
+def _shard_worker(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import dense_fp16_gemm_04_gb300 as g
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    row0, rows = g.shard_rows(3000, world, rank)
+    mine = torch.zeros(3000, dtype=torch.int64)
+    mine[row0:row0 + rows] = 1
+    dist.all_reduce(mine)                      # every row owned exactly once
+    out[rank] = bool((mine == 1).all())
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_split_rows_disjointly():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] and out[1]
