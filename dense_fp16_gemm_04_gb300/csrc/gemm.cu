@@ -211,11 +211,10 @@ struct Schedule {
 
 // Whole tiles are dealt round robin to U persistent units (U = CTA pairs or
 // CTAs that fit at once).  When T tiles are not a multiple of U the last wave
-// runs part-empty; then the last T % U + U tiles become a stream-K share
-// whose k-blocks are split evenly over the units (each unit runs its share
-// before its whole tiles), if the estimate (in k-block times per unit) says
-// it saves enough.  The testing mode 2 forces the share on any shape
-// (all tiles when T < 2U).
+// runs part-empty; then its T % U tiles become a stream-K share whose
+// k-blocks are split evenly over the units (each unit runs its share before
+// its whole tiles), if the estimate (in k-block times per unit) says it saves
+// enough.  The testing mode 2 forces the share on any shape.
 // Automatic choice, from measurements on GB300 (N = K = 8192 unless noted):
 // swapped roles when C has at most 64 rows (the tile then wastes no MMA rows
 // on padding and the work is spread over all SMs: 16 rows 32 us vs 42 us);
@@ -246,27 +245,31 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
   s.dp_tiles = T;
   s.sk_units = 0;
   s.sk_iters = 0;
-  // The share pays only when whole tiles follow it (T >= 2U): the partial-tile
+  // The share pays only when whole tiles follow it (T >= U): the partial-tile
   // fix-ups then overlap those tiles' main loops.  With nothing after it, the
-  // fix-ups end the kernel and cost more than the part-empty wave they save
-  // (measured: 1024 x 8192 x 8192 at 119 us with the share, 88 us without).
+  // fix-ups end the kernel and cost more than the part-empty wave they save.
   // With swapped roles a partial tile is small (128 x 16..64 fp32), so the
   // share is cheap even with no whole tiles after it: it is what spreads a
   // few tall tiles over every SM.
   const bool allowed = acc == GEMM_ACC_F32 && p->sk_ws && p->sk_count && KB > 0 &&
                        p->schedule_mode != 1 &&
-                       ((T % U != 0 && (T >= 2 * U || vi.swap)) || p->schedule_mode == 2);
+                       ((T % U != 0 && (T >= U || vi.swap)) || p->schedule_mode == 2);
   if (allowed) {
-    const int64_t sk_tiles = T >= U ? T % U + U : T;
+    // Only the tiles of the part-empty last wave are shared (all tiles when
+    // T < U): the smaller the share, the more of the work runs as whole tiles,
+    // whose concurrent units load the same k-blocks and share them in L2.
+    // Measured against sharing T % U + U tiles: 4096 x 4096 x 1024 +26%,
+    // 2048 x 8192 x 8192 +7%, 3000 x 5000 x 4104 +1.6%, 8192^3 unchanged.
+    const int64_t sk_tiles = T >= U ? (T % U != 0 ? T % U : U) : T;
     const int64_t dp = T - sk_tiles;
     const int64_t iters = sk_tiles * KB;
     // Forced mode (testing) lets units take as little as one k-block, so
     // tiles get many contributors.
     int64_t usk = iters / (p->schedule_mode == 2 ? 1 : kMinSkIters);
     if (usk > U) usk = U;
-    // At most about two contributors per tile: the last one reads the others'
-    // partial tiles, and that read grows with their number.
-    if (p->schedule_mode != 2 && !vi.swap && usk > 2 * sk_tiles) usk = 2 * sk_tiles;
+    // At most about four contributors per tile: the last one reads the
+    // others' partial tiles, and that read grows with their number.
+    if (p->schedule_mode != 2 && !vi.swap && usk > 4 * sk_tiles) usk = 4 * sk_tiles;
     const bool fits = static_cast<size_t>(sk_tiles * vi.ctas) <= p->sk_count_words;
     if (usk >= 2 && fits) {
       const double t_dp = static_cast<double>((T + U - 1) / U) * KB;

@@ -157,7 +157,7 @@ def test_cuda_graph_capture_and_replay():
     maps travel as kernel parameters and the stream-K counters reset
     themselves), so a captured call replays correctly, stream-K share
     included."""
-    M, N, K = 4096, 4096, 1024          # 256 pair tiles: whole tiles + a stream-K share
+    M, N, K = 4096, 4096, 4096          # 256 pair tiles: whole tiles + a stream-K share
     a, b = wl.draw(M, N, K, seed=37)
     ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
     c = torch.empty((M, N), dtype=torch.float16, device="cuda")

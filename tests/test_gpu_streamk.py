@@ -72,4 +72,4 @@ def test_auto_schedule_uses_the_tail_on_quantized_waves(plan):
     d = plan.describe(512, 512, 512)
     assert d["sk_units"] == 0           # fewer tiles than units: whole tiles
     d = plan.describe(1024, 8192, 8192)
-    assert d["sk_units"] == 0           # no whole wave would follow the share
+    assert d["sk_units"] > 0 and d["dp_tiles"] == d["units"]   # only the last wave is shared

@@ -35,11 +35,11 @@ def work(unit, units, T, KB, dp_tiles, sk_units):
 
 
 def schedule(T, KB, U):
-    sk_tiles = T % U + U if T >= U else T
+    sk_tiles = (T % U if T % U else U) if T >= U else T
     dp = T - sk_tiles
     usk = min(U, sk_tiles * KB // 16)
-    if usk > 2 * sk_tiles:
-        usk = 2 * sk_tiles
+    if usk > 4 * sk_tiles:
+        usk = 4 * sk_tiles
     return (U if dp > 0 else usk), dp, usk
 
 
