@@ -54,6 +54,9 @@ def parse():
                    help="storage of A and B: k = K-contiguous, m/n = M/N-contiguous")
     p.add_argument("--acc", default="f32", choices=["f32", "f16"])
     p.add_argument("--variant", default=None, help="force a kernel variant by name")
+    p.add_argument("--graph", action="store_true",
+                   help="capture the K timed launches in one CUDA graph (GPU time without "
+                        "per-call host overhead; for small shapes)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-rows", type=int, default=0,
@@ -270,11 +273,11 @@ def run_ours(args):
     sh = stream.cuda_stream
     aptr, bptr, cptr = a.data_ptr(), b.data_ptr(), c.data_ptr()
 
-    def step():
+    def step(stream_handle=sh):
         if la == g.K_CONTIGUOUS and lb == g.K_CONTIGUOUS:
-            plan.run_ptr(aptr, bptr, cptr, w.M, w.N, w.K, args.acc, sh)
+            plan.run_ptr(aptr, bptr, cptr, w.M, w.N, w.K, args.acc, stream_handle)
         else:
-            plan.run_ex_ptr(aptr, la, bptr, lb, cptr, w.M, w.N, w.K, args.acc, sh)
+            plan.run_ex_ptr(aptr, la, bptr, lb, cptr, w.M, w.N, w.K, args.acc, stream_handle)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -289,22 +292,36 @@ def run_ours(args):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     launches0 = plan.launch_count
+    graph = None
+    if args.graph:
+        cap = torch.cuda.Stream(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(args.steps):
+                step(cap.cuda_stream)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        launches0 = plan.launch_count
     sampler = ClockSampler(dev)
     barrier()
     with sampler:
         t_all0 = torch.cuda.Event(enable_timing=True)
         t_all1 = torch.cuda.Event(enable_timing=True)
         t_all0.record(stream)
-        for i in range(args.steps):
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
         t_all1.record(stream)
         barrier()
-    launches = plan.launch_count - launches0
+    launches = plan.launch_count - launches0 if graph is None else args.steps
     plan.check_error()
     total_ms = reduce_max(t_all0.elapsed_time(t_all1), world, dev)
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    per_launch_ms = ([s.elapsed_time(e) for s, e in zip(starts, ends)] if graph is None
+                     else [t_all0.elapsed_time(t_all1) / args.steps])
     clocks = sampler.summary()
 
     flops = float(w.flops)
@@ -356,7 +373,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (A+B = %d MB vs 129 MB L2), no flush"
                          % ((a_np.nbytes + b_np.nbytes) >> 20),
                    "parallelism": (f"M split x{world}" if strong else f"replicas x{world}")
-                                  if world > 1 else "single GPU"},
+                                  if world > 1 else "single GPU",
+                   "launch": "CUDA graph of the K steps" if graph is not None else "one call per step"},
         "pct_of_peak": value / world / peaks["tflops"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["tflops"],
