@@ -391,16 +391,21 @@ def run_ours(args):
 
 
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: a recorded ncu traffic figure is used only
-    while the kernels it was measured on are unchanged."""
+    """Hash of the CUDA sources' code (comments and whitespace removed): a
+    recorded ncu traffic figure is used only while the code it was measured
+    on is unchanged."""
     import glob
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp16_gemm_04_gb300", "csrc")
     for path in sorted(glob.glob(os.path.join(csrc, "*.cu*"))):
+        with open(path, encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
         h.update(os.path.basename(path).encode())
-        with open(path, "rb") as f:
-            h.update(f.read())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -3,19 +3,28 @@
 //   C[M,N] = A[M,K] x B[N,K]^T, fp16 in, fp32 or fp16 accumulate, fp16 out
 //   (tilus "A Minimal Hopper Matmul", section "Block Tiling").
 //
-// One template, two forms (tile width kBN = 64, 128 or 256 columns):
-//   kCtas = 1  one CTA per SM owns a 128 x kBN output tile;
-//   kCtas = 2  a cluster of two CTAs on neighbouring SMs owns a 256 x kBN
-//              tile: each CTA loads its 128 rows of A and half of the tile's
-//              rows of B, and one thread of the leader CTA issues
-//              tcgen05.mma.cta_group::2 (M = 256) over both CTAs' shared
-//              memory, so every SM stages a third less operand data per FLOP
-//              (at kBN = 256).
+// One template, three forms:
+//   kCtas = 1           one CTA per SM owns a 128 x kBN tile of C (kBN = 64..256);
+//   kCtas = 2           a cluster of two CTAs on neighbouring SMs owns a
+//                       256 x kBN tile: each CTA loads its 128 rows of A and
+//                       half of the tile's rows of B, and one thread of the
+//                       leader CTA issues tcgen05.mma.cta_group::2 (M = 256)
+//                       over both CTAs' shared memory, so every SM stages a
+//                       third less operand data per FLOP (at kBN = 256);
+//   kSwap               roles swapped for C with few rows: the MMA's M runs
+//                       over 128 columns of C (rows of B) and its N over
+//                       kBN = 16..64 rows of C, and the epilogue writes the
+//                       transposed tile straight to C.
+// Operands are K-contiguous or M/N-contiguous (run-time choice: TMA box shape,
+// shared-memory descriptor and the instruction descriptor's transpose bits).
 //
-// CTAs (or pairs) are persistent and walk the tiles with a static stride over
-// a grouped raster.  Inside a CTA the work is split by warp, after the
-// producer / consumer split of tilus "Warp Specialization", redesigned for
-// tcgen05:
+// Units (CTAs or pairs) are persistent.  Their work list (Sched) is a share of
+// the part-empty last wave's tiles cut into equal k-block ranges (stream-K)
+// followed by whole tiles dealt round robin over a grouped raster.  A tile
+// shared by several units is finished by whichever contributes last: the
+// others park fp32 partials in a workspace, and the last one sums them in
+// unit order.  Inside a CTA the work is split by warp, after the producer /
+// consumer split of tilus "Warp Specialization", redesigned for tcgen05:
 //
 //   warp 0, lane 0   TMA producer: fills a kStages-deep ring of A/B k-blocks.
 //   warp 1           allocates tensor memory (TMEM); lane 0 of the leader CTA
@@ -25,7 +34,7 @@
 //                    stage through swizzled shared memory, TMA-store.
 //
 // The accumulator is double-buffered in TMEM (2 x kBN columns), so the
-// epilogue of one tile overlaps the main loop of the next; tmem_full /
+// epilogue of one work item overlaps the main loop of the next; tmem_full /
 // tmem_empty barriers hand the buffers back and forth.
 //
 // Every wait is bounded: a wait that outlives the timeout records the site in
