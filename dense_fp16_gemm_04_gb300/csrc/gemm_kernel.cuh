@@ -26,10 +26,16 @@
 // unit order.  Inside a CTA the work is split by warp, after the producer /
 // consumer split of tilus "Warp Specialization", redesigned for tcgen05:
 //
-//   warp 0, lane 0   TMA producer: fills a kStages-deep ring of A/B k-blocks.
-//   warp 1           allocates tensor memory (TMEM); lane 0 of the leader CTA
+//   warps 0 and 6    TMA producers: a kStages-deep ring of k-blocks, warp 0
+//                    loading A and warp 6 loading B.
+//   warp 1           allocates tensor memory (TMEM); in the leader CTA it
 //                    issues every tcgen05.mma and releases each stage with
 //                    tcgen05.commit onto its "empty" mbarrier(s).
+// Producers and issuer run as whole, converged warps with one elected lane
+// issuing: measured on GB300, a lone divergent lane spends ~486 cycles per
+// k-block on 4 MMAs, a commit and a barrier test, a converged warp ~322; with
+// a 256-wide tile the tensor pipe needs 512 cycles per k-block, so only the
+// converged form keeps it fed.
 //   warps 2..5       epilogue: tcgen05.ld the accumulator, round to fp16,
 //                    stage through swizzled shared memory, TMA-store.
 //
@@ -185,7 +191,8 @@ struct GemmCfg {
   static constexpr int kSmemBytes = kOffFlag + 4 + 1024;   // + slack to align the base to 1024
   static constexpr int kPartialFloats = kBM * kBN;         // one CTA's share of a partial tile
   static constexpr int kTmemCols = 2 * kBN;
-  static constexpr int kThreads = 192;
+  static constexpr int kWarpProducerB = 6;  // warps 0 and 6 load A and B
+  static constexpr int kThreads = 224;
   static constexpr uint32_t kIdesc = ptx::idesc_f16(kTileM, kBN, !kAccF16);
 
   static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair");
@@ -241,6 +248,18 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
   return wait_slow<kClusterScope>(bar, parity, w, site, tile, honor_abort);
 }
 
+// Warp-collective wait: every lane waits and the warp agrees on the outcome,
+// so the code after it stays converged.  The producer and MMA roles run as
+// whole warps and let one elected lane issue: values computed in converged
+// code stay warp-uniform, and both the issue of tcgen05.mma / TMA and the
+// barrier test cost far fewer cycles than from a lone divergent lane.
+template <bool kClusterScope>
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Watch& w,
+                                              uint32_t site, int32_t tile,
+                                              bool honor_abort = true) {
+  return __all_sync(0xffffffffu, wait_bar<kClusterScope>(bar, parity, w, site, tile, honor_abort));
+}
+
 // Grouped raster: tiles are walked down a group of `group` tile-rows before
 // moving one tile-column right, so tiles in flight at the same time share A
 // rows and B rows in L2.  A bijection of [0, tiles_m*tiles_n).
@@ -293,7 +312,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     ptx::prefetch_tmap(&tmB);
     ptx::prefetch_tmap(&tmC);
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(bar_full(s), 1);
+      ptx::mbar_init(bar_full(s), 2);  // the A and B producers of the leader
       ptx::mbar_init(bar_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -316,9 +335,19 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffSlot);
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------ TMA producer --
+  if (warp == 0 || warp == Cfg::kWarpProducerB) {
+    {
+      // ----------------------------------------------------- TMA producers --
+      // One warp per operand: warp 0 loads A, warp kWarpProducerB loads B;
+      // the whole warp runs the loop and one elected lane issues the loads.
+      const bool is_a = warp == 0;
+      const CUtensorMap* tm = is_a ? &tmA : &tmB;
+      const bool mn = is_a ? args.a_mn != 0 : args.b_mn != 0;
+      const int mn_boxes = (is_a ? Cfg::kBM : Cfg::kBRows) / 64;
+      const uint32_t op_base = sb + (is_a ? Cfg::kOffA : Cfg::kOffB);
+      const uint32_t op_bytes = is_a ? Cfg::kABytes : Cfg::kBBytes;
+      // Both CTAs' bytes of this operand are counted on the leader's barrier.
+      const uint32_t op_tx = op_bytes * Cfg::kCtas;
       Sched sched(args, unit, units);
       WorkItem wi;
       int stage = 0;
@@ -329,56 +358,39 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       while (ok && sched.next(wi)) {
         int32_t mb, nb;
         raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
-        const int32_t a_row = mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM;
-        const int32_t b_row = nb * Cfg::kBN + static_cast<int32_t>(rank) * Cfg::kBRows;
+        const int32_t row = is_a ? mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM
+                                 : nb * Cfg::kBN + static_cast<int32_t>(rank) * Cfg::kBRows;
         for (int32_t kb = wi.kb0; kb < wi.kb1; ++kb) {
-          if (!wait_bar<kPair>(bar_empty(stage), phase ^ 1u, w, kSiteEmpty, wi.tile)) {
+          if (!wait_bar_warp<kPair>(bar_empty(stage), phase ^ 1u, w, kSiteEmpty, wi.tile)) {
             ok = false;
             break;
           }
           const bool skip = args.skip_kb == kb && first_item && unit == 0 && rank == 0;
-          if (!skip) {
+          if (!skip && ptx::elect_one()) {
+            const uint32_t dst = op_base + static_cast<uint32_t>(stage) * op_bytes;
+            // K-contiguous: one box of the tile's rows x 64 K-elements.
+            // M/N-contiguous: 64 x 64 boxes, 8 KB apart.
             if constexpr (kPair) {
-              // Both CTAs' bytes are counted on the leader's full barrier; the
-              // leader declares them all.
               const uint32_t full_leader = ptx::mapa(bar_full(stage), 0);
-              if (rank == 0) ptx::mbar_arrive_expect_tx(bar_full(stage), Cfg::kTxBytes);
-              if (args.a_mn) {
-#pragma unroll
-                for (int g = 0; g < Cfg::kBM / 64; ++g)
-                  ptx::tma_load_2d_pair(sA(stage) + g * 8192, &tmA, full_leader, a_row + 64 * g,
+              if (rank == 0) ptx::mbar_arrive_expect_tx(bar_full(stage), op_tx);
+              if (mn) {
+                for (int g = 0; g < mn_boxes; ++g)
+                  ptx::tma_load_2d_pair(dst + g * 8192, tm, full_leader, row + 64 * g,
                                         kb * Cfg::kBK);
               } else {
-                ptx::tma_load_2d_pair(sA(stage), &tmA, full_leader, kb * Cfg::kBK, a_row);
-              }
-              if (args.b_mn) {
-#pragma unroll
-                for (int g = 0; g < Cfg::kBRows / 64; ++g)
-                  ptx::tma_load_2d_pair(sB(stage) + g * 8192, &tmB, full_leader, b_row + 64 * g,
-                                        kb * Cfg::kBK);
-              } else {
-                ptx::tma_load_2d_pair(sB(stage), &tmB, full_leader, kb * Cfg::kBK, b_row);
+                ptx::tma_load_2d_pair(dst, tm, full_leader, kb * Cfg::kBK, row);
               }
             } else {
-              ptx::mbar_arrive_expect_tx(bar_full(stage), Cfg::kTxBytes);
-              if (args.a_mn) {
-#pragma unroll
-                for (int g = 0; g < Cfg::kBM / 64; ++g)
-                  ptx::tma_load_2d(sA(stage) + g * 8192, &tmA, bar_full(stage), a_row + 64 * g,
-                                   kb * Cfg::kBK);
+              ptx::mbar_arrive_expect_tx(bar_full(stage), op_tx);
+              if (mn) {
+                for (int g = 0; g < mn_boxes; ++g)
+                  ptx::tma_load_2d(dst + g * 8192, tm, bar_full(stage), row + 64 * g, kb * Cfg::kBK);
               } else {
-                ptx::tma_load_2d(sA(stage), &tmA, bar_full(stage), kb * Cfg::kBK, a_row);
-              }
-              if (args.b_mn) {
-#pragma unroll
-                for (int g = 0; g < Cfg::kBRows / 64; ++g)
-                  ptx::tma_load_2d(sB(stage) + g * 8192, &tmB, bar_full(stage), b_row + 64 * g,
-                                   kb * Cfg::kBK);
-              } else {
-                ptx::tma_load_2d(sB(stage), &tmB, bar_full(stage), kb * Cfg::kBK, b_row);
+                ptx::tma_load_2d(dst, tm, bar_full(stage), kb * Cfg::kBK, row);
               }
             }
           }
+          __syncwarp();
           ++fills;
           if (++stage == S) {
             stage = 0;
@@ -397,14 +409,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       for (int64_t f = fills - n; f < fills; ++f) {
         const int s = static_cast<int>(f % S);
         const uint32_t par = static_cast<uint32_t>((f / S) & 1);
-        if (ok) ok = wait_bar<kPair>(bar_empty(s), par, w, kSiteDrain, -1);
+        if (ok) ok = wait_bar_warp<kPair>(bar_empty(s), par, w, kSiteDrain, -1);
         if (!ok && rank == 0)
-          wait_bar<kPair>(bar_full(s), par, w, kSiteDrain, -1, /*honor_abort=*/false);
+          wait_bar_warp<kPair>(bar_full(s), par, w, kSiteDrain, -1, /*honor_abort=*/false);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
+    if (rank == 0) {
       // ------------------------------------------------------- MMA issuer --
+      // The whole warp runs the loop; one elected lane issues every
+      // tcgen05.mma and tcgen05.commit.
       const uint32_t idesc = Cfg::kIdesc | (args.a_mn ? ptx::kIdescAMnMajor : 0u) |
                              (args.b_mn ? ptx::kIdescBMnMajor : 0u);
       const uint64_t a_kstep = args.a_mn ? 128u : 2u;
@@ -418,14 +432,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       while (ok && sched.next(wi)) {
         const int buf = acc_iter & 1;
         const uint32_t use_par = static_cast<uint32_t>((acc_iter >> 1) & 1);
-        if (!wait_bar<kPair>(bar_tempty(buf), use_par ^ 1u, w, kSiteTmemEmpty, wi.tile)) {
+        if (!wait_bar_warp<kPair>(bar_tempty(buf), use_par ^ 1u, w, kSiteTmemEmpty, wi.tile)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kBN);
         for (int32_t kb = wi.kb0; kb < wi.kb1; ++kb) {
-          if (!wait_bar<kPair>(bar_full(stage), phase, w, kSiteFull, wi.tile)) {
+          if (!wait_bar_warp<kPair>(bar_full(stage), phase, w, kSiteFull, wi.tile)) {
             ok = false;
             break;
           }
@@ -434,37 +448,47 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                             : ptx::sw128_kmajor_desc(sA(stage));
           const uint64_t b_desc = args.b_mn ? ptx::sw128_mnmajor_desc(sB(stage))
                                             : ptx::sw128_kmajor_desc(sB(stage));
+          if (ptx::elect_one()) {
 #pragma unroll
-          for (int k = 0; k < Cfg::kBK / 16; ++k) {
-            // One 16-deep K step: +32 bytes inside the swizzled row (K-major)
-            // or +16 K-rows = 2048 bytes (MN-major); descriptors count in 16 B.
-            // The first step of the item overwrites the accumulator.
-            ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + a_kstep * k, b_desc + b_kstep * k, idesc,
-                                     (kb != wi.kb0 || k != 0) ? 1u : 0u);
+            for (int k = 0; k < Cfg::kBK / 16; ++k) {
+              // One 16-deep K step: +32 bytes inside the swizzled row
+              // (K-major) or +16 K-rows = 2048 bytes (MN-major); descriptors
+              // count in 16 B.  The first step of the item overwrites the
+              // accumulator.
+              ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + a_kstep * k, b_desc + b_kstep * k, idesc,
+                                       (kb != wi.kb0 || k != 0) ? 1u : 0u);
+            }
+            if constexpr (kPair)
+              ptx::mma_commit_pair(bar_empty(stage), 0x3);
+            else
+              ptx::mma_commit(bar_empty(stage));
           }
-          if constexpr (kPair)
-            ptx::mma_commit_pair(bar_empty(stage), 0x3);
-          else
-            ptx::mma_commit(bar_empty(stage));
+          __syncwarp();
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if constexpr (kPair)
-          ptx::mma_commit_pair(bar_tfull(buf), 0x3);
-        else
-          ptx::mma_commit(bar_tfull(buf));
+        if (ptx::elect_one()) {
+          if constexpr (kPair)
+            ptx::mma_commit_pair(bar_tfull(buf), 0x3);
+          else
+            ptx::mma_commit(bar_tfull(buf));
+        }
+        __syncwarp();
         ++acc_iter;
       }
-      // Every MMA this thread issued has finished before tensor memory is
-      // freed (bounded, whatever the abort state).
-      if constexpr (kPair)
-        ptx::mma_commit_pair(bar_mma_done, 0x1);
-      else
-        ptx::mma_commit(bar_mma_done);
-      wait_bar<kPair>(bar_mma_done, 0u, w, kSiteMmaDone, -1, /*honor_abort=*/false);
+      // Every MMA the elected lane issued has finished before tensor memory
+      // is freed (bounded, whatever the abort state).
+      if (ptx::elect_one()) {
+        if constexpr (kPair)
+          ptx::mma_commit_pair(bar_mma_done, 0x1);
+        else
+          ptx::mma_commit(bar_mma_done);
+      }
+      __syncwarp();
+      wait_bar_warp<kPair>(bar_mma_done, 0u, w, kSiteMmaDone, -1, /*honor_abort=*/false);
     }
   } else if constexpr (Cfg::kSwap) {
     // ---------------------------------------------- epilogue, swapped roles --

@@ -79,6 +79,19 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// One lane of the (fully converged) warp: true in exactly that lane.  The
+// same lane is chosen every time for the same set of active lanes, so a lane
+// elected for tcgen05.mma is also the one elected for its tcgen05.commit.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- clusters --
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
