@@ -84,6 +84,7 @@ def load():
             "gemm_plan_set_watchdog": (st, [vp, u64, i32]),
             "gemm_plan_set_variant": (st, [vp, i32]),
             "gemm_plan_set_schedule": (st, [vp, i32]),
+            "gemm_plan_set_pdl": (st, [vp, i32]),
             "gemm_plan_describe": (i32, [vp, i64, i64, i64, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int64)]),
             "gemm_variant_count": (i32, []),
@@ -222,6 +223,10 @@ class Plan:
         """'auto' (0), 'whole' tiles only (1) or 'streamk' whenever possible (2)."""
         mode = {"auto": 0, "whole": 1, "streamk": 2}.get(mode, mode)
         _check(self._lib.gemm_plan_set_schedule(self._h, int(mode)), "gemm_plan_set_schedule")
+
+    def set_pdl(self, enable: bool) -> None:
+        """Programmatic dependent launch of the GEMM kernel (default on)."""
+        _check(self._lib.gemm_plan_set_pdl(self._h, 1 if enable else 0), "gemm_plan_set_pdl")
 
     def describe(self, M, N, K, acc="f32") -> dict:
         """How gemm_run would lay out this call on the device."""

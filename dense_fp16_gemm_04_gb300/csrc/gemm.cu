@@ -104,6 +104,7 @@ struct gemm_plan_s {
   uint64_t timeout_ns = kDefaultTimeoutNs;
   int32_t skip_kb = -1;
   int32_t forced_variant = -1;
+  bool pdl = true;  // programmatic dependent launch of the GEMM kernel
   uint64_t launches = 0;
   uint64_t clock = 0;
   MapEntry maps[kMapCacheSize];
@@ -294,22 +295,29 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
 
 template <class Cfg>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                        const GemmArgs& args, int grid, cudaStream_t stream) {
+                        const GemmArgs& args, int grid, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
+  cfg.attrs = attr;
   cfg.numAttrs = 0;
   if (Cfg::kCtas == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = 2;
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    ++cfg.numAttrs;
+  }
+  if (pdl) {
+    // The kernel's set-up may overlap the end of the previous kernel in the
+    // stream; it waits for that kernel (griddepcontrol.wait) before touching
+    // global memory.
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
   }
   return cudaLaunchKernelEx(&cfg, gb300::gemm_tc_kernel<Cfg>, a, b, c, args);
 }
@@ -396,32 +404,32 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   cudaError_t e;
   switch (sch.variant) {
     case kVariantPair:
-      e = f32 ? launch_gemm<PairF32>(ma, mb, mc, args, grid, stream)
-              : launch_gemm<PairF16>(ma, mb, mc, args, grid, stream);
+      e = f32 ? launch_gemm<PairF32>(ma, mb, mc, args, grid, stream, p->pdl)
+              : launch_gemm<PairF16>(ma, mb, mc, args, grid, stream, p->pdl);
       break;
     case kVariantPair128:
-      e = f32 ? launch_gemm<Pair128F32>(ma, mb, mc, args, grid, stream)
-              : launch_gemm<Pair128F16>(ma, mb, mc, args, grid, stream);
+      e = f32 ? launch_gemm<Pair128F32>(ma, mb, mc, args, grid, stream, p->pdl)
+              : launch_gemm<Pair128F16>(ma, mb, mc, args, grid, stream, p->pdl);
       break;
     case kVariantSingle64:
-      e = f32 ? launch_gemm<Single64F32>(ma, mb, mc, args, grid, stream)
-              : launch_gemm<Single64F16>(ma, mb, mc, args, grid, stream);
+      e = f32 ? launch_gemm<Single64F32>(ma, mb, mc, args, grid, stream, p->pdl)
+              : launch_gemm<Single64F16>(ma, mb, mc, args, grid, stream, p->pdl);
       break;
     case kVariantSwap16:
-      e = f32 ? launch_gemm<Swap16F32>(ma, mb, mc, args, grid, stream)
-              : launch_gemm<Swap16F16>(ma, mb, mc, args, grid, stream);
+      e = f32 ? launch_gemm<Swap16F32>(ma, mb, mc, args, grid, stream, p->pdl)
+              : launch_gemm<Swap16F16>(ma, mb, mc, args, grid, stream, p->pdl);
       break;
     case kVariantSwap32:
-      e = f32 ? launch_gemm<Swap32F32>(ma, mb, mc, args, grid, stream)
-              : launch_gemm<Swap32F16>(ma, mb, mc, args, grid, stream);
+      e = f32 ? launch_gemm<Swap32F32>(ma, mb, mc, args, grid, stream, p->pdl)
+              : launch_gemm<Swap32F16>(ma, mb, mc, args, grid, stream, p->pdl);
       break;
     case kVariantSwap64:
-      e = f32 ? launch_gemm<Swap64F32>(ma, mb, mc, args, grid, stream)
-              : launch_gemm<Swap64F16>(ma, mb, mc, args, grid, stream);
+      e = f32 ? launch_gemm<Swap64F32>(ma, mb, mc, args, grid, stream, p->pdl)
+              : launch_gemm<Swap64F16>(ma, mb, mc, args, grid, stream, p->pdl);
       break;
     default:
-      e = f32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, stream)
-              : launch_gemm<SingleF16>(ma, mb, mc, args, grid, stream);
+      e = f32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, stream, p->pdl)
+              : launch_gemm<SingleF16>(ma, mb, mc, args, grid, stream, p->pdl);
   }
   ++p->launches;
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -589,6 +597,12 @@ int32_t gemm_plan_describe(gemm_plan_t p, int64_t M, int64_t N, int64_t K, gemm_
   out[4] = s.sk_units;
   out[5] = s.sk_iters;
   return 0;
+}
+
+gemm_status_t gemm_plan_set_pdl(gemm_plan_t p, int32_t enable) {
+  if (!p || (enable != 0 && enable != 1)) return GEMM_ERR_INVALID_ARG;
+  p->pdl = enable != 0;
+  return GEMM_OK;
 }
 
 gemm_status_t gemm_plan_set_variant(gemm_plan_t p, int32_t v) {
@@ -881,7 +895,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   // The watchdog record must start at zero; the array keeps the last call's
   // contents, so clear it on the caller's stream before the launch.
   if (cudaMemsetAsync(d.scratch, 0, kNoAllocRecordBytes, st) != cudaSuccess) return GEMM_ERR_CUDA;
-  cudaError_t e = acc == GEMM_ACC_F32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, st)
-                                      : launch_gemm<SingleF16>(ma, mb, mc, args, grid, st);
+  cudaError_t e = acc == GEMM_ACC_F32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, st, false)
+                                      : launch_gemm<SingleF16>(ma, mb, mc, args, grid, st, false);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -334,6 +334,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffSlot);
+  // Everything above touches only this CTA's shared and tensor memory, so
+  // with programmatic dependent launch it overlaps the end of the previous
+  // kernel in the stream.  Global memory (A, B, C, the stream-K workspace)
+  // is touched only after that kernel has completed; the next kernel may
+  // start its own set-up on SMs as they free up.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   if (warp == 0 || warp == Cfg::kWarpProducerB) {
     {

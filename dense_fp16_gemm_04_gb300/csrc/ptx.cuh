@@ -79,6 +79,15 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Programmatic dependent launch.  griddep_wait: returns once the kernels this
+// grid depends on have completed and their memory writes are visible (at
+// once when there are none).  griddep_launch_dependents: this CTA no longer
+// holds back the launch of the next kernel in the stream.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // One lane of the (fully converged) warp: true in exactly that lane.  The
 // same lane is chosen every time for the same set of active lanes, so a lane
 // elected for tcgen05.mma is also the one elected for its tcgen05.commit.

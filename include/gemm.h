@@ -158,6 +158,14 @@ GEMM_API gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout
  * stay deterministic); fp16 accumulation always uses whole tiles. */
 GEMM_API gemm_status_t gemm_plan_set_schedule(gemm_plan_t plan, int32_t mode);
 
+/* Programmatic dependent launch (default 1 = on): the GEMM kernel is launched
+ * so that its set-up (barriers, tensor-memory allocation) may overlap the end
+ * of the previous kernel in the stream; it waits for that kernel to complete
+ * before reading or writing any global memory, so results never depend on
+ * this setting.  0 launches with plain stream ordering.  GEMM_ERR_INVALID_ARG
+ * for any other value.  No counterpart in the source pages (a launch detail). */
+GEMM_API gemm_status_t gemm_plan_set_pdl(gemm_plan_t plan, int32_t enable);
+
 /* How gemm_run would lay out this call: out[0] variant, out[1] CTAs launched,
  * out[2] units (CTAs or CTA pairs), out[3] tiles handed out whole, out[4]
  * units sharing the stream-K tail (0 = none), out[5] k-blocks in the tail.
