@@ -336,9 +336,36 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffSlot);
   // Everything above touches only this CTA's shared and tensor memory, so
   // with programmatic dependent launch it overlaps the end of the previous
-  // kernel in the stream.  Global memory (A, B, C, the stream-K workspace)
-  // is touched only after that kernel has completed; the next kernel may
-  // start its own set-up on SMs as they free up.
+  // kernel in the stream.  So does an L2 prefetch of the first k-blocks each
+  // producer will load: it reads nothing into the CTA, and L2 stays coherent
+  // with that kernel's writes, so the loads after the wait below see its
+  // results either way; it takes the DRAM latency of the first stages off
+  // the kernel's start.  Global memory (A, B, C, the stream-K workspace) is
+  // read or written only after the previous kernel has completed; the next
+  // kernel may start its own set-up on SMs as they free up.
+  if (warp == 0 || warp == Cfg::kWarpProducerB) {
+    Sched sched(args, unit, units);
+    WorkItem wi;
+    if (sched.next(wi) && ptx::elect_one()) {
+      const bool is_a = warp == 0;
+      const CUtensorMap* tm = is_a ? &tmA : &tmB;
+      const bool mn = is_a ? args.a_mn != 0 : args.b_mn != 0;
+      const int mn_boxes = (is_a ? Cfg::kBM : Cfg::kBRows) / 64;
+      int32_t mb, nb;
+      raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
+      const int32_t row = is_a ? mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM
+                               : nb * Cfg::kBN + static_cast<int32_t>(rank) * Cfg::kBRows;
+      const int32_t kb_end = wi.kb1 < wi.kb0 + S ? wi.kb1 : wi.kb0 + S;
+      for (int32_t kb = wi.kb0; kb < kb_end; ++kb) {
+        if (mn) {
+          for (int g = 0; g < mn_boxes; ++g) ptx::tma_prefetch_l2_2d(tm, row + 64 * g, kb * Cfg::kBK);
+        } else {
+          ptx::tma_prefetch_l2_2d(tm, kb * Cfg::kBK, row);
+        }
+      }
+    }
+    __syncwarp();
+  }
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
