@@ -44,12 +44,16 @@ using Swap32F32 = GemmCfg<1, 10, false, 32, true>;
 using Swap32F16 = GemmCfg<1, 10, true, 32, true>;
 using Swap64F32 = GemmCfg<1, 8, false, 64, true>;
 using Swap64F16 = GemmCfg<1, 8, true, 64, true>;
+// Two CTA pairs per cluster sharing the A block of their tile-row (multicast).
+using PairMcF32 = GemmCfg<2, 6, false, 256, false, 2>;
+using PairMcF16 = GemmCfg<2, 6, true, 256, false, 2>;
 
 struct VariantInfo {
   const char* name;
-  int ctas;            // CTAs per tile (cluster size)
-  int tile_m, tile_n;  // output tile (rows x columns of C) owned by one CTA or CTA pair
-  int box_a_rows;      // rows of A each CTA loads per stage
+  int ctas;            // CTAs per unit (cluster size)
+  int tile_m, tile_n;  // output tile (rows x columns of C) owned by one unit: a CTA, a CTA
+                       // pair, or two pairs side by side in N
+  int box_a_rows;      // rows of A each CTA loads per stage (K-contiguous A)
   int box_b_rows;      // rows of B each CTA loads per stage
   bool swap;           // MMA roles swapped: the kernel's tiles run over (N, M)
 };
@@ -61,7 +65,8 @@ constexpr int kVariantSingle64 = 3;
 constexpr int kVariantSwap16 = 4;
 constexpr int kVariantSwap32 = 5;
 constexpr int kVariantSwap64 = 6;
-constexpr int kNumVariants = 7;
+constexpr int kVariantPairMc = 7;
+constexpr int kNumVariants = 8;
 constexpr VariantInfo kVariants[kNumVariants] = {
     {"tc_pair_256x256_s6", 2, 256, 256, 128, 128, false},
     {"tc_single_128x256_s4", 1, 128, 256, 128, 256, false},
@@ -70,6 +75,7 @@ constexpr VariantInfo kVariants[kNumVariants] = {
     {"tc_swap_16x128_s11", 1, 16, 128, 16, 128, true},
     {"tc_swap_32x128_s10", 1, 32, 128, 32, 128, true},
     {"tc_swap_64x128_s8", 1, 64, 128, 64, 128, true},
+    {"tc_pair_mc_256x256_s6", 4, 256, 512, 64, 128, false},
 };
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s for any single wait
@@ -91,6 +97,7 @@ struct gemm_plan_s {
   int device = 0;
   int num_sms = 0;
   int max_pairs = 0;  // CTA pairs of the pair kernel that fit on the device at once
+  int max_quads = 0;  // two-pair clusters of the multicast kernel that fit at once
   // Stream-K workspace, allocated once at plan creation: partial fp32 tiles
   // (2 slots per unit) and per-tile contribution counters (kept at zero
   // between launches by the kernel itself).
@@ -224,13 +231,19 @@ struct Schedule {
 // Very small problems (fewer 256 x 256 tiles than a quarter of the resident
 // pairs) also go to the 128 x 64 tiles, which spread their few k-blocks over
 // more SMs (512^3: 11.1 us vs 13.2 us; 1024^3: 11.2 us vs 13.4 us).
-int auto_variant(int64_t M, int64_t N, int max_pairs) {
+// K-contiguous rows whose pitch is not a multiple of 128 bytes (K % 64 != 0)
+// make every 128-byte TMA row straddle two L2 lines, doubling the load
+// requests each SM issues; there two pairs share A by multicast, halving A's
+// requests (3000 x 5000 x 4104: 1514 vs 1311 TFLOP/s).  On aligned rows the
+// fewer resident units cost more than the multicast saves (8192^3: -6%).
+int auto_variant(int64_t M, int64_t N, int64_t K, bool k_major, int max_pairs, int max_quads) {
   if (M <= 16) return kVariantSwap16;
   if (M <= 32) return kVariantSwap32;
   if (M <= 64) return kVariantSwap64;
   if (M <= 128) return kVariantSingle64;
   const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
   if (4 * pair_tiles < max_pairs) return kVariantSingle64;
+  if (k_major && K % 64 != 0 && max_quads > 0) return kVariantPairMc;
   return kVariantPair;
 }
 
@@ -238,13 +251,15 @@ int auto_variant(int64_t M, int64_t N, int max_pairs) {
 // take K-contiguous operands only).
 Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
                        bool mn = false) {
-  int v = p->forced_variant >= 0 ? p->forced_variant : auto_variant(M, N, p->max_pairs);
+  int v = p->forced_variant >= 0 ? p->forced_variant
+                                 : auto_variant(M, N, K, !mn, p->max_pairs, p->max_quads);
   if (mn && kVariants[v].swap) v = M <= 128 ? kVariantSingle64 : kVariantPair;
+  if (kVariants[v].ctas == 4 && p->max_quads < 1) v = kVariantPair;
   if (kVariants[v].ctas == 2 && p->max_pairs < 1) v = kVariantSingle;
   const VariantInfo& vi = kVariants[v];
   const int64_t T = tiles_of(vi, M, N);
   const int64_t KB = (K + 63) / 64;
-  const int64_t U = vi.ctas == 2 ? p->max_pairs : p->num_sms;
+  const int64_t U = vi.ctas == 4 ? p->max_quads : vi.ctas == 2 ? p->max_pairs : p->num_sms;
   Schedule s;
   s.variant = v;
   s.units = T < U ? T : U;
@@ -304,9 +319,9 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 0;
-  if (Cfg::kCtas == 2) {
+  if (Cfg::kClusterCtas > 1) {
     attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
-    attr[cfg.numAttrs].val.clusterDim.x = 2;
+    attr[cfg.numAttrs].val.clusterDim.x = Cfg::kClusterCtas;
     attr[cfg.numAttrs].val.clusterDim.y = 1;
     attr[cfg.numAttrs].val.clusterDim.z = 1;
     ++cfg.numAttrs;
@@ -322,15 +337,16 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   return cudaLaunchKernelEx(&cfg, gb300::gemm_tc_kernel<Cfg>, a, b, c, args);
 }
 
+// Clusters of the kernel (CTA pairs, or two-pair clusters) resident at once.
 template <class Cfg>
-int max_active_pairs() {
+int max_active_clusters() {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(2, 1, 1);
+  cfg.gridDim = dim3(Cfg::kClusterCtas, 1, 1);
   cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = Cfg::kClusterCtas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -406,6 +422,10 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
     case kVariantPair:
       e = f32 ? launch_gemm<PairF32>(ma, mb, mc, args, grid, stream, p->pdl)
               : launch_gemm<PairF16>(ma, mb, mc, args, grid, stream, p->pdl);
+      break;
+    case kVariantPairMc:
+      e = f32 ? launch_gemm<PairMcF32>(ma, mb, mc, args, grid, stream, p->pdl)
+              : launch_gemm<PairMcF16>(ma, mb, mc, args, grid, stream, p->pdl);
       break;
     case kVariantPair128:
       e = f32 ? launch_gemm<Pair128F32>(ma, mb, mc, args, grid, stream, p->pdl)
@@ -514,16 +534,19 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
       set_smem_attr<Single64F32>() != cudaSuccess || set_smem_attr<Single64F16>() != cudaSuccess ||
       set_smem_attr<Swap16F32>() != cudaSuccess || set_smem_attr<Swap16F16>() != cudaSuccess ||
       set_smem_attr<Swap32F32>() != cudaSuccess || set_smem_attr<Swap32F16>() != cudaSuccess ||
-      set_smem_attr<Swap64F32>() != cudaSuccess || set_smem_attr<Swap64F16>() != cudaSuccess) {
+      set_smem_attr<Swap64F32>() != cudaSuccess || set_smem_attr<Swap64F16>() != cudaSuccess ||
+      set_smem_attr<PairMcF32>() != cudaSuccess || set_smem_attr<PairMcF16>() != cudaSuccess) {
     delete p;
     return GEMM_ERR_CUDA;
   }
   {
-    int m = max_active_pairs<PairF32>();
-    for (int n : {max_active_pairs<PairF16>(), max_active_pairs<Pair128F32>(),
-                  max_active_pairs<Pair128F16>()})
+    int m = max_active_clusters<PairF32>();
+    for (int n : {max_active_clusters<PairF16>(), max_active_clusters<Pair128F32>(),
+                  max_active_clusters<Pair128F16>()})
       m = n < m ? n : m;
     p->max_pairs = m;
+    const int q0 = max_active_clusters<PairMcF32>(), q1 = max_active_clusters<PairMcF16>();
+    p->max_quads = q0 < q1 ? q0 : q1;
   }
   if (cudaMalloc(&p->d_err, 4 * sizeof(uint32_t)) != cudaSuccess) {
     delete p;

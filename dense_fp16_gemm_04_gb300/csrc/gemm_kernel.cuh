@@ -160,9 +160,16 @@ struct Sched {
 };
 
 // Tile configuration.  kCtas CTAs cooperate on one tile of kTileM x kBN.
-template <int kCtas_, int kStages_, bool kAccF16_, int kBN_ = 256, bool kSwap_ = false>
+template <int kCtas_, int kStages_, bool kAccF16_, int kBN_ = 256, bool kSwap_ = false,
+          int kMc_ = 1>
 struct GemmCfg {
   static constexpr int kCtas = kCtas_;
+  // kMc = 2: a cluster holds two CTA pairs working on neighbouring tiles of
+  // the same tile-row; the pairs share the tile-row's A block, each CTA
+  // loading half of its 128 rows and multicasting it to the CTA in the same
+  // position of the other pair, so every SM requests half as many A bytes.
+  static constexpr int kMc = kMc_;
+  static constexpr int kClusterCtas = kCtas * kMc;
   // Swapped roles (for small M): the MMA's "A" operand is a 128-row tile of B
   // and its "B" operand a kBN-row tile of A, so D = tile of C^T.
   static constexpr bool kSwap = kSwap_;
@@ -196,6 +203,8 @@ struct GemmCfg {
   static constexpr uint32_t kIdesc = ptx::idesc_f16(kTileM, kBN, !kAccF16);
 
   static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair");
+  static_assert(kMc == 1 || (kMc == 2 && kCtas == 2 && !kSwap),
+                "A multicast between two CTA pairs only");
   static_assert(kSwap ? (kCtas == 1 && (kBN == 16 || kBN == 32 || kBN == 64))
                       : (kBN == 64 || kBN == 128 || kBN == 256),
                 "tile width: 64, 128 or 256; 16, 32 or 64 with swapped roles (one CTA)");
@@ -291,8 +300,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const uint32_t sb = ptx::smem_addr(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Position of this CTA in its pair and of the pair in the grid.
+  // Position of this CTA in its cluster, in its pair, and of the pair in the
+  // cluster; units (CTAs, pairs or two-pair clusters) in the grid.
   const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
+  const uint32_t cta = rank & 1u;       // 0: the pair's leader, which issues the MMAs
+  const uint32_t pair = rank >> 1;      // which pair of a two-pair cluster
+  const uint32_t leader = rank & ~1u;   // cluster rank of this pair's leader
+  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << Cfg::kClusterCtas) - 1u);
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << leader);
+  // Tile column of this pair's tile, from the unit's tile column.
+  auto tile_nb = [&](int32_t nbx) { return nbx * Cfg::kMc + static_cast<int32_t>(pair); };
   const int32_t unit = kPair ? static_cast<int32_t>(ptx::cluster_id_x()) : static_cast<int32_t>(blockIdx.x);
   const int32_t units = kPair ? static_cast<int32_t>(ptx::num_clusters_x()) : static_cast<int32_t>(gridDim.x);
 
@@ -313,7 +330,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     ptx::prefetch_tmap(&tmC);
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar_full(s), 2);  // the A and B producers of the leader
-      ptx::mbar_init(bar_empty(s), 1);
+      ptx::mbar_init(bar_empty(s), Cfg::kMc);  // one tcgen05.commit per pair reading the stage
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(bar_tfull(b), 1);
@@ -350,15 +367,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const bool is_a = warp == 0;
       const CUtensorMap* tm = is_a ? &tmA : &tmB;
       const bool mn = is_a ? args.a_mn != 0 : args.b_mn != 0;
-      const int mn_boxes = (is_a ? Cfg::kBM : Cfg::kBRows) / 64;
-      int32_t mb, nb;
-      raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
-      const int32_t row = is_a ? mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM
-                               : nb * Cfg::kBN + static_cast<int32_t>(rank) * Cfg::kBRows;
-      const int32_t kb_end = wi.kb1 < wi.kb0 + S ? wi.kb1 : wi.kb0 + S;
+      int32_t mb, nbx;
+      raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nbx);
+      // This CTA's part of the operand: A rows [row, row + rows), or B rows.
+      const int32_t rows = is_a ? Cfg::kBM / Cfg::kMc : Cfg::kBRows;
+      const int32_t row = is_a ? mb * Cfg::kTileM + static_cast<int32_t>(cta) * Cfg::kBM +
+                                     static_cast<int32_t>(pair) * rows
+                               : tile_nb(nbx) * Cfg::kBN + static_cast<int32_t>(cta) * Cfg::kBRows;
+      // (With two pairs per cluster, the second pair's tile may lie wholly
+      // beyond N: its B loads then only fill zeros, nothing to prefetch.)
+      const bool in_range = Cfg::kMc == 1 || is_a || tile_nb(nbx) * Cfg::kBN < args.N;
+      const int32_t kb_end = !in_range ? wi.kb0 : wi.kb1 < wi.kb0 + S ? wi.kb1 : wi.kb0 + S;
       for (int32_t kb = wi.kb0; kb < kb_end; ++kb) {
         if (mn) {
-          for (int g = 0; g < mn_boxes; ++g) ptx::tma_prefetch_l2_2d(tm, row + 64 * g, kb * Cfg::kBK);
+          for (int g = 0; g < rows / 64; ++g) ptx::tma_prefetch_l2_2d(tm, row + 64 * g, kb * Cfg::kBK);
         } else {
           ptx::tma_prefetch_l2_2d(tm, kb * Cfg::kBK, row);
         }
@@ -377,10 +399,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const bool is_a = warp == 0;
       const CUtensorMap* tm = is_a ? &tmA : &tmB;
       const bool mn = is_a ? args.a_mn != 0 : args.b_mn != 0;
-      const int mn_boxes = (is_a ? Cfg::kBM : Cfg::kBRows) / 64;
-      const uint32_t op_base = sb + (is_a ? Cfg::kOffA : Cfg::kOffB);
+      // With A multicast this CTA loads one half of its pair's A rows (pair
+      // p of the cluster the p-th half) into both pairs' shared memory.
+      const bool mc = is_a && Cfg::kMc == 2;
+      const int32_t rows = is_a ? Cfg::kBM / Cfg::kMc : Cfg::kBRows;
+      const int mn_boxes = rows / 64;
       const uint32_t op_bytes = is_a ? Cfg::kABytes : Cfg::kBBytes;
-      // Both CTAs' bytes of this operand are counted on the leader's barrier.
+      const uint32_t op_base = sb + (is_a ? Cfg::kOffA : Cfg::kOffB) +
+                               (mc ? pair * (op_bytes / Cfg::kMc) : 0u);
+      const uint16_t mc_mask = static_cast<uint16_t>(0x5u << cta);  // this position in both pairs
+      // Both CTAs' bytes of this operand are counted on the pair leader's
+      // barrier (with multicast: the bytes landing in either CTA of the pair,
+      // whichever pair loaded them).
       const uint32_t op_tx = op_bytes * Cfg::kCtas;
       Sched sched(args, unit, units);
       WorkItem wi;
@@ -390,10 +420,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       bool ok = true;
       bool first_item = true;
       while (ok && sched.next(wi)) {
-        int32_t mb, nb;
-        raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
-        const int32_t row = is_a ? mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM
-                                 : nb * Cfg::kBN + static_cast<int32_t>(rank) * Cfg::kBRows;
+        int32_t mb, nbx;
+        raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nbx);
+        const int32_t row = is_a ? mb * Cfg::kTileM + static_cast<int32_t>(cta) * Cfg::kBM +
+                                       static_cast<int32_t>(pair) * rows
+                                 : tile_nb(nbx) * Cfg::kBN + static_cast<int32_t>(cta) * Cfg::kBRows;
         for (int32_t kb = wi.kb0; kb < wi.kb1; ++kb) {
           if (!wait_bar_warp<kPair>(bar_empty(stage), phase ^ 1u, w, kSiteEmpty, wi.tile)) {
             ok = false;
@@ -405,9 +436,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             // K-contiguous: one box of the tile's rows x 64 K-elements.
             // M/N-contiguous: 64 x 64 boxes, 8 KB apart.
             if constexpr (kPair) {
-              const uint32_t full_leader = ptx::mapa(bar_full(stage), 0);
-              if (rank == 0) ptx::mbar_arrive_expect_tx(bar_full(stage), op_tx);
-              if (mn) {
+              const uint32_t full_leader = ptx::mapa(bar_full(stage), leader);
+              if (cta == 0) ptx::mbar_arrive_expect_tx(bar_full(stage), op_tx);
+              if (mc) {
+                if (mn) {
+                  for (int g = 0; g < mn_boxes; ++g)
+                    ptx::tma_load_2d_pair_mc(dst + g * 8192, tm, full_leader, row + 64 * g,
+                                             kb * Cfg::kBK, mc_mask);
+                } else {
+                  ptx::tma_load_2d_pair_mc(dst, tm, full_leader, kb * Cfg::kBK, row, mc_mask);
+                }
+              } else if (mn) {
                 for (int g = 0; g < mn_boxes; ++g)
                   ptx::tma_load_2d_pair(dst + g * 8192, tm, full_leader, row + 64 * g,
                                         kb * Cfg::kBK);
@@ -444,12 +483,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int s = static_cast<int>(f % S);
         const uint32_t par = static_cast<uint32_t>((f / S) & 1);
         if (ok) ok = wait_bar_warp<kPair>(bar_empty(s), par, w, kSiteDrain, -1);
-        if (!ok && rank == 0)
+        if (!ok && cta == 0)
           wait_bar_warp<kPair>(bar_full(s), par, w, kSiteDrain, -1, /*honor_abort=*/false);
       }
     }
   } else if (warp == 1) {
-    if (rank == 0) {
+    if (cta == 0) {
       // ------------------------------------------------------- MMA issuer --
       // The whole warp runs the loop; one elected lane issues every
       // tcgen05.mma and tcgen05.commit.
@@ -492,8 +531,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + a_kstep * k, b_desc + b_kstep * k, idesc,
                                        (kb != wi.kb0 || k != 0) ? 1u : 0u);
             }
+            // The stage is free once every pair reading it is done: with A
+            // multicast both pairs' issuers release it in all four CTAs.
             if constexpr (kPair)
-              ptx::mma_commit_pair(bar_empty(stage), 0x3);
+              ptx::mma_commit_pair(bar_empty(stage), kClusterMask);
             else
               ptx::mma_commit(bar_empty(stage));
           }
@@ -506,7 +547,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (!ok) break;
         if (ptx::elect_one()) {
           if constexpr (kPair)
-            ptx::mma_commit_pair(bar_tfull(buf), 0x3);
+            ptx::mma_commit_pair(bar_tfull(buf), pair_mask);
           else
             ptx::mma_commit(bar_tfull(buf));
         }
@@ -517,7 +558,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // is freed (bounded, whatever the abort state).
       if (ptx::elect_one()) {
         if constexpr (kPair)
-          ptx::mma_commit_pair(bar_mma_done, 0x1);
+          ptx::mma_commit_pair(bar_mma_done, static_cast<uint16_t>(1u << rank));
         else
           ptx::mma_commit(bar_mma_done);
       }
@@ -647,11 +688,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const uint32_t stage_base = sb + Cfg::kOffEpi + static_cast<uint32_t>(q * 2 * Cfg::kEpiBufBytes);
     // tmem_empty lives in the leader CTA: every epilogue warp of the pair
     // arrives there.
-    const uint32_t tempty_bar0 = kPair ? ptx::mapa(bar_tempty(0), 0) : bar_tempty(0);
+    const uint32_t tempty_bar0 = kPair ? ptx::mapa(bar_tempty(0), leader) : bar_tempty(0);
     volatile uint32_t* last_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffFlag);
     // This CTA's share of unit u's partial tile in slot `slot`.
     auto partial = [&](int32_t u, int32_t slot) {
-      return args.sk_ws + (static_cast<size_t>(u * 2 + slot) * Cfg::kCtas + rank) *
+      return args.sk_ws + (static_cast<size_t>(u * 2 + slot) * Cfg::kClusterCtas + rank) *
                               static_cast<size_t>(Cfg::kPartialFloats);
     };
     Sched sched(args, unit, units);
@@ -659,8 +700,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     uint32_t stores = 0;
     int32_t acc_iter = 0;
     while (sched.next(wi)) {
-      int32_t mb, nb;
-      raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
+      int32_t mb, nbx;
+      raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nbx);
+      const int32_t nb = tile_nb(nbx);
       const int buf = acc_iter & 1;
       const uint32_t use_par = static_cast<uint32_t>((acc_iter >> 1) & 1);
       ++acc_iter;
@@ -673,7 +715,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * Cfg::kBN);
-      const int32_t row0 = mb * Cfg::kTileM + static_cast<int32_t>(rank) * Cfg::kBM + q * 32;
+      const int32_t row0 = mb * Cfg::kTileM + static_cast<int32_t>(cta) * Cfg::kBM + q * 32;
       const bool split = !Cfg::kAccF16 && wi.splits > 1;
       if (split) {
         // Stream-K tail tile shared with other units.  (a) Park this unit's
@@ -708,7 +750,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         __threadfence();
         ptx::named_barrier_sync(1, 32 * Cfg::kEpiWarps);
         if (threadIdx.x == 64) {
-          uint32_t* cnt = args.sk_count + static_cast<size_t>(wi.sk_tile) * Cfg::kCtas + rank;
+          uint32_t* cnt = args.sk_count + static_cast<size_t>(wi.sk_tile) * Cfg::kClusterCtas + rank;
           const uint32_t before = atomicAdd(cnt, 1u);
           const bool last = before == static_cast<uint32_t>(wi.splits - 1);
           if (last) *cnt = 0u;

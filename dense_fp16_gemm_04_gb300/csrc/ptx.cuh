@@ -159,6 +159,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Pair form with multicast: the same box lands at offset `dst` in the shared
+// memory of every CTA in `cta_mask` (bit i = cluster rank i), and for each of
+// them the transaction bytes are counted on the barrier at `bar`'s offset in
+// the leader of that CTA's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* m,
+                                                    uint32_t bar, int32_t c0, int32_t c1,
+                                                    uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
+      : "memory");
+}
+
 // Bring the box at (c0, c1) into L2 only: nothing is written to shared
 // memory and nothing is waited for.
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t c0, int32_t c1) {

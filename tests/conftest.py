@@ -82,10 +82,10 @@ def assert_close(got, ref, acc, what=""):
 # library by test_abi_host.py::test_variant_table).
 VARIANTS = ["tc_pair_256x256_s6", "tc_single_128x256_s4", "tc_pair_256x128_s8",
             "tc_single_128x64_s8", "tc_swap_16x128_s11", "tc_swap_32x128_s10",
-            "tc_swap_64x128_s8"]
+            "tc_swap_64x128_s8", "tc_pair_mc_256x256_s6"]
 # The variants built for large M (the swapped-roles ones, made for a few rows
 # of C, would take minutes on the full-size squares).
-VARIANTS_WIDE = VARIANTS[:4]
+VARIANTS_WIDE = VARIANTS[:4] + VARIANTS[7:]
 
 
 @pytest.fixture(scope="session")
