@@ -353,44 +353,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffSlot);
   // Everything above touches only this CTA's shared and tensor memory, so
   // with programmatic dependent launch it overlaps the end of the previous
-  // kernel in the stream.  So does an L2 prefetch of the first k-blocks each
-  // producer will load: it reads nothing into the CTA, and L2 stays coherent
-  // with that kernel's writes, so the loads after the wait below see its
-  // results either way; it takes the DRAM latency of the first stages off
-  // the kernel's start.  Global memory (A, B, C, the stream-K workspace) is
-  // read or written only after the previous kernel has completed; the next
-  // kernel may start its own set-up on SMs as they free up.
-  if (warp == 0 || warp == Cfg::kWarpProducerB) {
-    Sched sched(args, unit, units);
-    WorkItem wi;
-    if (sched.next(wi) && ptx::elect_one()) {
-      const bool is_a = warp == 0;
-      const CUtensorMap* tm = is_a ? &tmA : &tmB;
-      const bool mn = is_a ? args.a_mn != 0 : args.b_mn != 0;
-      int32_t mb, nbx;
-      raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nbx);
-      // This CTA's part of the operand: A rows [row, row + rows), or B rows.
-      const int32_t rows = is_a ? Cfg::kBM / Cfg::kMc : Cfg::kBRows;
-      const int32_t row = is_a ? mb * Cfg::kTileM + static_cast<int32_t>(cta) * Cfg::kBM +
-                                     static_cast<int32_t>(pair) * rows
-                               : tile_nb(nbx) * Cfg::kBN + static_cast<int32_t>(cta) * Cfg::kBRows;
-      // (With two pairs per cluster, the second pair's tile may lie wholly
-      // beyond N: its B loads then only fill zeros, nothing to prefetch.)
-      const bool in_range = Cfg::kMc == 1 || is_a || tile_nb(nbx) * Cfg::kBN < args.N;
-      const int32_t kb_end = !in_range ? wi.kb0 : wi.kb1 < wi.kb0 + S ? wi.kb1 : wi.kb0 + S;
-      for (int32_t kb = wi.kb0; kb < kb_end; ++kb) {
-        if (mn) {
-          for (int g = 0; g < rows / 64; ++g) ptx::tma_prefetch_l2_2d(tm, row + 64 * g, kb * Cfg::kBK);
-        } else {
-          ptx::tma_prefetch_l2_2d(tm, kb * Cfg::kBK, row);
-        }
-      }
-    }
-    __syncwarp();
-  }
-  ptx::griddep_wait();
-  ptx::griddep_launch_dependents();
-
+  // kernel in the stream.  Global memory (A, B, C, the stream-K workspace) is
+  // read or written only after that kernel has completed (griddepcontrol.wait
+  // in the producer and epilogue roles; the MMA issuer touches none); the
+  // next kernel may start its own set-up on SMs as they free up.
   if (warp == 0 || warp == Cfg::kWarpProducerB) {
     {
       // ----------------------------------------------------- TMA producers --
@@ -412,19 +378,48 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // barrier (with multicast: the bytes landing in either CTA of the pair,
       // whichever pair loaded them).
       const uint32_t op_tx = op_bytes * Cfg::kCtas;
+      // First row of this CTA's part of the operand in work item `it`: A rows
+      // [row, row + rows) or B rows.
+      auto row_of = [&](const WorkItem& it) {
+        int32_t mb, nbx;
+        raster(it.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nbx);
+        return is_a ? mb * Cfg::kTileM + static_cast<int32_t>(cta) * Cfg::kBM +
+                          static_cast<int32_t>(pair) * rows
+                    : tile_nb(nbx) * Cfg::kBN + static_cast<int32_t>(cta) * Cfg::kBRows;
+      };
       Sched sched(args, unit, units);
       WorkItem wi;
+      // The first work item is worked out before the wait for the previous
+      // kernel, so that after it only the loads themselves remain.  So is an
+      // L2 prefetch of the item's first k-blocks: it reads nothing into the
+      // CTA, and L2 stays coherent with the previous kernel's writes, so the
+      // loads after the wait see its results either way; it takes the DRAM
+      // latency of the first stages off the kernel's start.
+      bool have = sched.next(wi);
+      int32_t row = have ? row_of(wi) : 0;
+      if (have && ptx::elect_one()) {
+        // (With two pairs per cluster, the second pair's tile may lie wholly
+        // beyond N: its B loads then only fill zeros, nothing to prefetch.)
+        const bool in_range = Cfg::kMc == 1 || is_a || row < args.N;
+        const int32_t kb_end = !in_range ? wi.kb0 : wi.kb1 < wi.kb0 + S ? wi.kb1 : wi.kb0 + S;
+        for (int32_t kb = wi.kb0; kb < kb_end; ++kb) {
+          if (mn) {
+            for (int g = 0; g < mn_boxes; ++g)
+              ptx::tma_prefetch_l2_2d(tm, row + 64 * g, kb * Cfg::kBK);
+          } else {
+            ptx::tma_prefetch_l2_2d(tm, kb * Cfg::kBK, row);
+          }
+        }
+      }
+      __syncwarp();
+      ptx::griddep_wait();
+      ptx::griddep_launch_dependents();
       int stage = 0;
       uint32_t phase = 0;
       int64_t fills = 0;
       bool ok = true;
       bool first_item = true;
-      while (ok && sched.next(wi)) {
-        int32_t mb, nbx;
-        raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nbx);
-        const int32_t row = is_a ? mb * Cfg::kTileM + static_cast<int32_t>(cta) * Cfg::kBM +
-                                       static_cast<int32_t>(pair) * rows
-                                 : tile_nb(nbx) * Cfg::kBN + static_cast<int32_t>(cta) * Cfg::kBRows;
+      for (; ok && have; have = sched.next(wi), row = have ? row_of(wi) : 0) {
         for (int32_t kb = wi.kb0; kb < wi.kb1; ++kb) {
           if (!wait_bar_warp<kPair>(bar_empty(stage), phase ^ 1u, w, kSiteEmpty, wi.tile)) {
             ok = false;
@@ -567,6 +562,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
   } else if constexpr (Cfg::kSwap) {
     // ---------------------------------------------- epilogue, swapped roles --
+    ptx::griddep_wait();  // writes C and the workspace
     // The MMA computed a tile of C^T = B x A^T: TMEM lane = column n of C,
     // TMEM column = row m of C.  Each thread owns one column n and stores its
     // kBN values down it; for a fixed m the warp's 32 lanes write 32
@@ -683,6 +679,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue --
+    ptx::griddep_wait();  // writes C and the workspace
     const int q = warp & 3;  // this warp may touch TMEM lanes 32q .. 32q+31 only
     const int row_in_cta = q * 32 + lane;
     const uint32_t stage_base = sb + Cfg::kOffEpi + static_cast<uint32_t>(q * 2 * Cfg::kEpiBufBytes);
