@@ -137,6 +137,20 @@ def test_host_entry_point_ragged_many_chunks(plan):
     assert_close(got, oracle.gemm_rows_f64(a, b, rows), "f32", "run_host ragged")
 
 
+def test_host_entry_point_many_row_chunks(plan):
+    """M = 9000 is cut into nine row chunks (1024 rows each, the last one
+    ragged), each multiplied as soon as it has arrived; every row of C must
+    come back, checked on sampled rows and on the last rows."""
+    M, N, K = 9000, 520, 1032
+    a, b = wl.draw(M, N, K, seed=72)
+    hc = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    plan.run_host(torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory(), hc)
+    rows = np.unique(np.concatenate([wl.sample_indices(M, 64, 73), np.arange(M - 8, M)]))
+    got = hc.numpy()[rows].astype(np.float64)
+    assert_close(got, oracle.gemm_rows_f64(a, b, rows), "f32", "run_host nine chunks")
+    assert np.isfinite(hc.numpy()).all()
+
+
 def test_gemm_convenience_wrapper(plan):
     a, b = wl.draw(256, 264, 128, seed=35)
     c = g.gemm(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
