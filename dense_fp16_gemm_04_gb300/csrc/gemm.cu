@@ -81,11 +81,15 @@ constexpr VariantInfo kVariants[kNumVariants] = {
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s for any single wait
 constexpr int kGroupM = 8;                             // raster group height, tiles
 constexpr int kMapCacheSize = 32;
-constexpr int kHostChunks = 32;       // most row chunks gemm_run_host pipelines
+// gemm_run_host's pipeline: at most kHostChunksA row chunks of A and
+// kHostChunksB of B, and at most kHostBlocks blocks of C.
+constexpr int kHostChunksA = 32;
+constexpr int kHostChunksB = 8;
+constexpr int kHostBlocks = 64;
 
 struct MapEntry {
   const void* ptr;
-  uint64_t rows, cols;
+  uint64_t rows, cols, pitch;
   uint32_t box_rows, box_cols;
   uint64_t stamp;
   CUtensorMap map;
@@ -121,11 +125,11 @@ struct gemm_plan_s {
   void* dC = nullptr;
   size_t capA = 0, capB = 0, capC = 0;
   // gemm_run_host's copy-in, compute and copy-out streams and their events
-  // (created on first use).
+  // (created on first use): one per input chunk, one per block of C.
   cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
   cudaEvent_t ev_start = nullptr;
-  cudaEvent_t ev_in[kHostChunks] = {};
-  cudaEvent_t ev_comp[kHostChunks] = {};
+  cudaEvent_t ev_in[kHostChunksA + kHostChunksB] = {};
+  cudaEvent_t ev_comp[kHostBlocks] = {};
 };
 
 namespace {
@@ -144,13 +148,15 @@ struct DeviceGuard {
   }
 };
 
+// Row-major fp16 [rows, cols] whose rows are `pitch` elements apart (0: cols).
 bool get_map(gemm_plan_s* p, CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols,
-             uint32_t box_rows, uint32_t box_cols) {
+             uint32_t box_rows, uint32_t box_cols, uint64_t pitch = 0) {
+  if (pitch == 0) pitch = cols;
   MapEntry* victim = &p->maps[0];
   for (int i = 0; i < kMapCacheSize; ++i) {
     MapEntry& e = p->maps[i];
-    if (e.stamp && e.ptr == ptr && e.rows == rows && e.cols == cols && e.box_rows == box_rows &&
-        e.box_cols == box_cols) {
+    if (e.stamp && e.ptr == ptr && e.rows == rows && e.cols == cols && e.pitch == pitch &&
+        e.box_rows == box_rows && e.box_cols == box_cols) {
       e.stamp = ++p->clock;
       *out = e.map;
       return true;
@@ -159,14 +165,14 @@ bool get_map(gemm_plan_s* p, CUtensorMap* out, const void* ptr, uint64_t rows, u
   }
   // Row-major fp16 [rows, cols]: dimension 0 is the contiguous one.
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {pitch * 2};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   // Rows whose pitch is not a multiple of 128 bytes straddle L2 lines; then
   // promoting each request to 256 bytes costs more than it saves (measured
   // ~6% slower at K = 4104), so promote by 128 bytes there.
-  const CUtensorMapL2promotion promo = (cols * 2) % 128 == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-                                                            : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+  const CUtensorMapL2promotion promo = (pitch * 2) % 128 == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                                             : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
   CUresult r = p->encode(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr),
                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -177,6 +183,7 @@ bool get_map(gemm_plan_s* p, CUtensorMap* out, const void* ptr, uint64_t rows, u
   victim->ptr = ptr;
   victim->rows = rows;
   victim->cols = cols;
+  victim->pitch = pitch;
   victim->box_rows = box_rows;
   victim->box_cols = box_cols;
   victim->stamp = ++p->clock;
@@ -359,10 +366,14 @@ int max_active_clusters() {
   return n;
 }
 
+// C = A x B^T on device buffers.  C's rows are `ldc` elements apart (0: N),
+// so a block of a larger C can be written in place (K > 0 only).
 gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, int64_t M,
                          int64_t N, int64_t K, gemm_acc_t acc, cudaStream_t stream,
-                         int la = GEMM_K_CONTIGUOUS, int lb = GEMM_K_CONTIGUOUS) {
+                         int la = GEMM_K_CONTIGUOUS, int lb = GEMM_K_CONTIGUOUS, int64_t ldc = 0) {
+  if (ldc == 0) ldc = N;
   if (K == 0) {
+    if (ldc != N) return GEMM_ERR_INVALID_ARG;
     const int64_t n16 = M * N * 2 / 16;
     const int64_t blocks = (n16 + 255) / 256;
     gb300::gemm_zero_fill<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0,
@@ -384,7 +395,7 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   const bool maps_ok =
       (a_mn ? get_map(p, &ma, A, K, M, 64, 64) : get_map(p, &ma, A, M, K, vi.box_a_rows, 64)) &&
       (b_mn ? get_map(p, &mb, B, K, N, 64, 64) : get_map(p, &mb, B, N, K, vi.box_b_rows, 64)) &&
-      get_map(p, &mc, C, M, N, 32, 64);
+      get_map(p, &mc, C, M, N, 32, 64, static_cast<uint64_t>(ldc));
   if (!maps_ok) return GEMM_ERR_CUDA;
 
   GemmArgs args;
@@ -401,7 +412,7 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
     args.tiles_n = static_cast<int32_t>((N + vi.tile_n - 1) / vi.tile_n);
   }
   args.C = static_cast<uint16_t*>(C);
-  args.ldc = N;
+  args.ldc = ldc;
   args.a_mn = a_mn ? 1 : 0;
   args.b_mn = b_mn ? 1 : 0;
   args.num_kb = static_cast<int32_t>((K + 63) / 64);
@@ -585,10 +596,10 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t p) {
   for (cudaStream_t st : {p->s_in, p->s_comp, p->s_out})
     if (st) cudaStreamDestroy(st);
   if (p->ev_start) cudaEventDestroy(p->ev_start);
-  for (int i = 0; i < kHostChunks; ++i) {
-    if (p->ev_in[i]) cudaEventDestroy(p->ev_in[i]);
-    if (p->ev_comp[i]) cudaEventDestroy(p->ev_comp[i]);
-  }
+  for (cudaEvent_t e : p->ev_in)
+    if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : p->ev_comp)
+    if (e) cudaEventDestroy(e);
   if (p->dA) cudaFree(p->dA);
   if (p->dB) cudaFree(p->dB);
   if (p->dC) cudaFree(p->dC);
@@ -737,41 +748,90 @@ gemm_status_t gemm_run_host(gemm_plan_t p, const void* A, const void* B, void* C
               cudaStreamCreateWithFlags(&p->s_comp, cudaStreamNonBlocking) == cudaSuccess &&
               cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&p->ev_start, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; ok && i < kHostChunks; ++i)
-      ok = cudaEventCreateWithFlags(&p->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&p->ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
+    for (cudaEvent_t& e : p->ev_in)
+      ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+    for (cudaEvent_t& e : p->ev_comp)
+      ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
     if (!ok) return GEMM_ERR_CUDA;
   }
-  // Pipeline over row chunks of A and C: B goes in first, then chunk i of A
-  // is copied in while chunk i-1 is multiplied and chunk i-2 of C is copied
-  // out, so the host links in both directions and the tensor cores overlap.
-  // Work starts after everything already queued on the caller's stream.
-  // Chunks of whole 256-row tiles: at least four when M allows, at most 1024
-  // rows each (finer chunks shorten the exposed first and last chunk, but
-  // much smaller GEMMs lose more than that: 8192^3 +5% with 1024-row chunks,
-  // 16384^3 +7%, 4096^3 -3% with 512-row chunks), and no more than
-  // kHostChunks.
-  auto tiles256 = [](int64_t r) { return (r + 255) / 256 * 256; };
-  int64_t rows = std::min<int64_t>(1024, tiles256((M + 3) / 4));
-  rows = std::max<int64_t>(rows, tiles256((M + kHostChunks - 1) / kHostChunks));
-  const int chunks = static_cast<int>((M + rows - 1) / rows);
   auto& d = *p;
   bool ok = cudaEventRecord(d.ev_start, static_cast<cudaStream_t>(stream)) == cudaSuccess &&
-            cudaStreamWaitEvent(d.s_in, d.ev_start, 0) == cudaSuccess;
-  if (ok && K > 0) ok = cudaMemcpyAsync(d.dB, B, bB, cudaMemcpyHostToDevice, d.s_in) == cudaSuccess;
-  for (int i = 0; ok && i < chunks; ++i) {
-    const int64_t r0 = i * rows, mi = std::min<int64_t>(rows, M - r0);
-    const char* a_h = static_cast<const char*>(A) + r0 * K * 2;
-    char* a_d = static_cast<char*>(d.dA) + r0 * K * 2;
-    char* c_d = static_cast<char*>(d.dC) + r0 * N * 2;
-    char* c_h = static_cast<char*>(C) + r0 * N * 2;
-    if (K > 0) ok = cudaMemcpyAsync(a_d, a_h, mi * K * 2, cudaMemcpyHostToDevice, d.s_in) == cudaSuccess;
-    ok = ok && cudaEventRecord(d.ev_in[i], d.s_in) == cudaSuccess &&
-         cudaStreamWaitEvent(d.s_comp, d.ev_in[i], 0) == cudaSuccess;
-    if (ok && (s = run_device(p, a_d, d.dB, c_d, mi, N, K, acc, d.s_comp)) != GEMM_OK) break;
-    ok = ok && cudaEventRecord(d.ev_comp[i], d.s_comp) == cudaSuccess &&
-         cudaStreamWaitEvent(d.s_out, d.ev_comp[i], 0) == cudaSuccess &&
-         cudaMemcpyAsync(c_h, c_d, mi * N * 2, cudaMemcpyDeviceToHost, d.s_out) == cudaSuccess;
+            cudaStreamWaitEvent(d.s_in, d.ev_start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(d.s_comp, d.ev_start, 0) == cudaSuccess;
+  if (ok && K == 0) {  // the empty sum: zeros, no input to copy
+    ok = (s = run_device(p, nullptr, nullptr, d.dC, M, N, 0, acc, d.s_comp)) == GEMM_OK &&
+         cudaEventRecord(d.ev_comp[0], d.s_comp) == cudaSuccess &&
+         cudaStreamWaitEvent(d.s_out, d.ev_comp[0], 0) == cudaSuccess &&
+         cudaMemcpyAsync(C, d.dC, bC, cudaMemcpyDeviceToHost, d.s_out) == cudaSuccess;
+  }
+  // The pipeline.  A is cut into row chunks A_i and B into row chunks B_j
+  // (whole 256-row tiles); the copy-in stream sends them alternately, in
+  // proportion, block C_ij = A_i B_j^T is multiplied as soon as both of its
+  // chunks have arrived, and the copy-out stream returns each block (a
+  // strided 2-D copy) while later chunks are still coming in, so both
+  // directions of the host link and the tensor cores overlap.  Work starts
+  // after everything already queued on the caller's stream.
+  // Compute time over copy-in time goes as MN / (M + N), whatever K.  Below
+  // ~6144 the host link is the bound: B whole and A in chunks of at most
+  // 1024 rows (at least four), so only the first and last chunk are exposed
+  // (8192^3: 662 TFLOP/s; cutting B too gave 664, 4096^3 277 vs 294).  Above
+  // it the tensor cores matter as much, and cutting both operands into
+  // ~2048-row chunks lets them start after two chunks instead of all of B
+  // (16384^3: 1252 vs 1086).
+  auto tiles256 = [](int64_t r) { return (r + 255) / 256 * 256; };
+  int64_t rows = 0, cols = 0;
+  int mc = 0, nc = 0;
+  if (K > 0) {
+    if (static_cast<double>(M) * static_cast<double>(N) / static_cast<double>(M + N) >= 6144.0) {
+      auto split = [&](int64_t n, int64_t& per) {
+        const int64_t parts = std::min<int64_t>(kHostChunksB, std::max<int64_t>(1, (n + 1024) / 2048));
+        per = tiles256((n + parts - 1) / parts);
+        return static_cast<int>((n + per - 1) / per);
+      };
+      mc = split(M, rows);
+      nc = split(N, cols);
+    } else {
+      rows = std::min<int64_t>(1024, tiles256((M + 3) / 4));
+      rows = std::max<int64_t>(rows, tiles256((M + kHostChunksA - 1) / kHostChunksA));
+      mc = static_cast<int>((M + rows - 1) / rows);
+      cols = N;
+      nc = 1;
+    }
+  }
+  bool have_a[kHostChunksA] = {}, have_b[kHostChunksB] = {};
+  int ia = 0, ib = 0, blocks = 0;
+  for (int step = 0; ok && step < mc + nc; ++step) {
+    // Next chunk: the operand with the smaller fraction sent so far.
+    const bool take_a = ib == nc || (ia < mc && static_cast<int64_t>(ia) * nc <= static_cast<int64_t>(ib) * mc);
+    const int idx = take_a ? ia++ : ib++;
+    const int64_t r0 = idx * (take_a ? rows : cols);
+    const int64_t n = std::min<int64_t>(take_a ? rows : cols, (take_a ? M : N) - r0);
+    const char* src = static_cast<const char*>(take_a ? A : B) + r0 * K * 2;
+    char* dst = static_cast<char*>(take_a ? d.dA : d.dB) + r0 * K * 2;
+    ok = cudaMemcpyAsync(dst, src, static_cast<size_t>(n) * K * 2, cudaMemcpyHostToDevice, d.s_in) ==
+             cudaSuccess &&
+         cudaEventRecord(d.ev_in[step], d.s_in) == cudaSuccess &&
+         cudaStreamWaitEvent(d.s_comp, d.ev_in[step], 0) == cudaSuccess;
+    (take_a ? have_a : have_b)[idx] = true;
+    // Every block this chunk completes.
+    for (int other = 0; ok && other < (take_a ? nc : mc); ++other) {
+      if (!(take_a ? have_b : have_a)[other]) continue;
+      const int i = take_a ? idx : other, j = take_a ? other : idx;
+      const int64_t m0 = i * rows, mi = std::min<int64_t>(rows, M - m0);
+      const int64_t n0 = j * cols, nj = std::min<int64_t>(cols, N - n0);
+      const size_t c_off = static_cast<size_t>(m0 * N + n0) * 2;
+      if ((s = run_device(p, static_cast<char*>(d.dA) + m0 * K * 2,
+                          static_cast<char*>(d.dB) + n0 * K * 2, static_cast<char*>(d.dC) + c_off, mi,
+                          nj, K, acc, d.s_comp, GEMM_K_CONTIGUOUS, GEMM_K_CONTIGUOUS, N)) != GEMM_OK) {
+        ok = false;
+        break;
+      }
+      cudaEvent_t e = d.ev_comp[blocks++];
+      ok = cudaEventRecord(e, d.s_comp) == cudaSuccess &&
+           cudaStreamWaitEvent(d.s_out, e, 0) == cudaSuccess &&
+           cudaMemcpy2DAsync(static_cast<char*>(C) + c_off, N * 2, static_cast<char*>(d.dC) + c_off,
+                             N * 2, nj * 2, mi, cudaMemcpyDeviceToHost, d.s_out) == cudaSuccess;
+    }
   }
   const bool synced = cudaStreamSynchronize(d.s_in) == cudaSuccess &&
                       cudaStreamSynchronize(d.s_comp) == cudaSuccess &&

@@ -151,6 +151,24 @@ def test_host_entry_point_many_row_chunks(plan):
     assert np.isfinite(hc.numpy()).all()
 
 
+def test_host_entry_point_two_dimensional_blocks(plan):
+    """MN / (M + N) >= 6144 switches gemm_run_host to cutting both A and B
+    into row chunks: here 6 x 6 blocks of C with ragged last blocks in both
+    directions, each multiplied as its two chunks arrive and copied back
+    with a strided copy.  Every element must come back: sampled rows and
+    columns against the oracle, all finite."""
+    M, N, K = 12500, 13000, 72
+    a, b = wl.draw(M, N, K, seed=74)
+    hc = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    plan.run_host(torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory(), hc)
+    c = hc.numpy()
+    assert np.isfinite(c).all()
+    rows = np.unique(np.concatenate([wl.sample_indices(M, 48, 75), [0, 2303, 2304, M - 1]]))
+    cols = np.unique(np.concatenate([wl.sample_indices(N, 48, 76), [0, 2303, 2304, N - 1]]))
+    assert_close(c[rows].astype(np.float64), oracle.gemm_rows_f64(a, b, rows), "f32", "2-D rows")
+    assert_close(c[:, cols].astype(np.float64), oracle.gemm_cols_f64(a, b, cols), "f32", "2-D cols")
+
+
 def test_gemm_convenience_wrapper(plan):
     a, b = wl.draw(256, 264, 128, seed=35)
     c = g.gemm(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
