@@ -73,3 +73,40 @@ def test_auto_schedule_uses_the_tail_on_quantized_waves(plan):
     assert d["sk_units"] == 0           # fewer tiles than units: whole tiles
     d = plan.describe(1024, 8192, 8192)
     assert d["sk_units"] > 0 and d["dp_tiles"] == d["units"]   # only the last wave is shared
+
+
+def test_auto_schedule_swapped_roles(plan):
+    """Few tall tiles (C with at most 64 rows): each tile is cut into the
+    same whole number of k-pieces when its partial tiles are large or there
+    are pieces to spare, else the units' ranges run on across tiles."""
+    d = plan.describe(64, 8192, 8192)         # 64 tiles of 128 columns: 2 pieces each
+    assert d["variant"] == "tc_swap_64x128_s8" and d["sk_units"] == 128 and d["dp_tiles"] == 0
+    d = plan.describe(16, 8192, 8192)         # 2 x 64 tiles <= 152 units: 2 pieces each
+    assert d["sk_units"] == 128
+    d = plan.describe(48, 12288, 8192)        # 96 tiles, one piece each: whole tiles
+    assert d["sk_units"] == 0 and d["units"] == 96 and d["dp_tiles"] == 96
+    d = plan.describe(16, 16384, 16384)       # 128 tiles of 16 rows: ranges over all units
+    assert d["sk_units"] == d["units"] and d["sk_iters"] == 128 * 256
+
+
+def test_every_share_unit_has_work():
+    """The fix-up counts on every unit of a stream-K share contributing: no
+    schedule may give a unit of the share an empty k-range.  Checked on the
+    host-side layout (no launch) for every variant and schedule mode over a
+    sweep of shapes, tiny K and few tiles included."""
+    import dense_fp16_gemm_04_gb300 as g
+    shapes = [(8, 120, 264), (16, 128, 64), (64, 8192, 1024), (64, 8192, 8192), (16, 8192, 8192),
+              (48, 12288, 8192), (16, 16384, 16384), (300, 520, 328), (1000, 776, 4104),
+              (4096, 4096, 1024), (4096, 4096, 4096), (3000, 5000, 4104), (129, 264, 1032),
+              (8, 8, 4096), (2000, 40, 256), (16, 1024, 65536), (256, 256, 8)]
+    for variant in g.variant_names():
+        for mode in ("auto", "streamk"):
+            p = g.Plan(0)
+            p.set_variant(variant)
+            p.set_schedule(mode)
+            for M, N, K in shapes:
+                d = p.describe(M, N, K)
+                if d["sk_units"]:
+                    floor = 1 if mode == "streamk" else 16
+                    assert d["sk_iters"] >= floor * d["sk_units"], (variant, mode, (M, N, K), d)
+            p.close()
