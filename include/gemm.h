@@ -115,11 +115,13 @@ GEMM_API gemm_status_t gemm_run_ex(gemm_plan_t plan, const void* A, gemm_layout_
                                    int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
                                    void* stream);
 
-/* Same product on HOST buffers, synchronous: copies B and then row chunks of
- * A to device staging buffers owned by the plan (grown with cudaMalloc on
- * first use of a larger shape), multiplies each chunk as soon as it has
- * arrived and copies its rows of C back while later chunks are still in
- * flight (three internal streams, created on first use).  The work starts
+/* Same product on HOST buffers, synchronous: copies row chunks of A and B
+ * to device staging buffers owned by the plan (grown with cudaMalloc on
+ * first use of a larger shape), multiplies each block of C as soon as the
+ * chunks it needs have arrived, and copies the block back while later
+ * chunks are still in flight (three internal streams, created on first
+ * use).  B travels whole unless M*N/(M+N) >= 6144, when the multiplies are
+ * long enough to start them before all of B has arrived.  The work starts
  * after everything already queued on `stream`; the call returns when C is
  * filled.  A, B, C are host pointers (pinned memory gives full copy
  * bandwidth and the overlap; pageable memory works but is slower).  Same
