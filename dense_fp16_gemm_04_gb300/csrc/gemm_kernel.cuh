@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int g = 0; g < Cfg::kBN / 16; ++g) {
           uint32_t v[16];
           ptx::tmem_ld_32x32b_x16(t_row + g * 16, v);
-          ptx::tmem_wait_ld();
+          ptx::tmem_wait_ld(v);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             ptx::st_global_v4(own + static_cast<size_t>(g * 4 + j) * (Cfg::kBM * 4), v[4 * j],
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if constexpr (Cfg::kAccF16) {
             uint32_t v[8];
             ptx::tmem_ld_32x32b_x8_pack16(t_row + g * 16, v);
-            ptx::tmem_wait_ld();
+            ptx::tmem_wait_ld(v);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const __half2 h = *reinterpret_cast<const __half2*>(&v[i]);
@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           } else {
             uint32_t v[16];
             ptx::tmem_ld_32x32b_x16(t_row + g * 16, v);
-            ptx::tmem_wait_ld();
+            ptx::tmem_wait_ld(v);
 #pragma unroll
             for (int i = 0; i < 16; ++i) acc[g * 16 + i] = __uint_as_float(v[i]);
           }
@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int c = 0; c < Cfg::kBN / 32; ++c) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(t_row + c * 32, v);
-          ptx::tmem_wait_ld();
+          ptx::tmem_wait_ld(v);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             ptx::st_global_v4(own + static_cast<size_t>(c * 8 + j) * (Cfg::kBM * 4), v[4 * j],
@@ -785,12 +785,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         } else {
           if constexpr (Cfg::kAccF16) {
             ptx::tmem_ld_32x32b_x32_pack16(t_row + c * 64, packed);
-            ptx::tmem_wait_ld();
+            ptx::tmem_wait_ld(packed);
           } else {
             uint32_t v0[32], v1[32];
             ptx::tmem_ld_32x32b_x32(t_row + c * 64, v0);
             ptx::tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
-            ptx::tmem_wait_ld();
+            ptx::tmem_wait_ld(v0);
+            ptx::tmem_regs_ready(v1);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               packed[i] = pack_half2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));

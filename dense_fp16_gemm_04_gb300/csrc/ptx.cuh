@@ -297,6 +297,24 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Registers a tcgen05.ld writes hold their values only once tcgen05.wait::ld
+// has returned, but the compiler sees them defined at the load.  Passing each
+// through an empty asm placed after the wait (volatile asm statements keep
+// their order) makes every later use depend on the wait.  No instruction is
+// emitted.
+template <int N>
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// tcgen05.wait::ld, and the registers of `r` usable from here on.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[N]) {
+  tmem_wait_ld();
+  tmem_regs_ready(r);
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives lane
 // (base lane + t), columns col .. col+31.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
