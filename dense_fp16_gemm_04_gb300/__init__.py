@@ -85,6 +85,7 @@ def load():
             "gemm_plan_set_variant": (st, [vp, i32]),
             "gemm_plan_set_schedule": (st, [vp, i32]),
             "gemm_plan_set_pdl": (st, [vp, i32]),
+            "gemm_plan_set_tile_order": (st, [vp, i32]),
             "gemm_plan_describe": (i32, [vp, i64, i64, i64, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int64)]),
             "gemm_variant_count": (i32, []),
@@ -223,6 +224,11 @@ class Plan:
         """'auto' (0), 'whole' tiles only (1) or 'streamk' whenever possible (2)."""
         mode = {"auto": 0, "whole": 1, "streamk": 2}.get(mode, mode)
         _check(self._lib.gemm_plan_set_schedule(self._h, int(mode)), "gemm_plan_set_schedule")
+
+    def set_tile_order(self, mode) -> None:
+        """'auto' (0), 'static' round robin (1) or 'dynamic' whenever possible (2)."""
+        mode = {"auto": 0, "static": 1, "dynamic": 2}.get(mode, mode)
+        _check(self._lib.gemm_plan_set_tile_order(self._h, int(mode)), "gemm_plan_set_tile_order")
 
     def set_pdl(self, enable: bool) -> None:
         """Programmatic dependent launch of the GEMM kernel (default on)."""

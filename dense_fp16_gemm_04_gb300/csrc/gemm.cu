@@ -108,6 +108,10 @@ struct gemm_plan_s {
   float* sk_ws = nullptr;
   uint32_t* sk_count = nullptr;
   size_t sk_count_words = 0;
+  // Dynamic tile order: ticket and finished-unit counters (two words after
+  // the stream-K counters, kept at zero between launches by the kernel).
+  uint32_t* tile_ctr = nullptr;
+  int32_t tile_order = 0;  // 0 automatic, 1 static round robin, 2 dynamic when possible
   int32_t schedule_mode = 0;  // 0 auto, 1 whole tiles only, 2 stream-K tail whenever possible
   EncodeTiledFn encode = nullptr;
   uint32_t* d_err = nullptr;  // 4-word watchdog record
@@ -222,6 +226,7 @@ struct Schedule {
   int64_t dp_tiles;   // tiles handed out whole
   int64_t sk_units;   // units sharing the stream-K tail (0 = none)
   int64_t sk_iters;   // k-blocks in the tail
+  bool dyn;           // whole tiles after each unit's first come in the dynamic order
 };
 
 // Whole tiles are dealt round robin to U persistent units (U = CTA pairs or
@@ -273,6 +278,7 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
   s.dp_tiles = T;
   s.sk_units = 0;
   s.sk_iters = 0;
+  s.dyn = false;
   // The share pays only when whole tiles follow it (T >= U): the partial-tile
   // fix-ups then overlap those tiles' main loops.  With nothing after it, the
   // fix-ups end the kernel and cost more than the part-empty wave they save.
@@ -325,6 +331,17 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
       }
     }
   }
+  // Dynamic order of whole tiles for long runs of waves: with the static
+  // round robin, units that run slightly faster drift ahead (at 16384^3 the
+  // start of a unit's 40th tile spreads over 120 us, more than a tile), the
+  // tiles in flight spread over several waves and their shared operands are
+  // evicted from L2 between uses: DRAM reads 18.7 GB per launch static, 11.8
+  // GB dynamic, which under the power cap buys SM clock (16384^3 +3 to +5%).
+  // Its hand-off costs ~0.5% when the clock is not capped (8192^3: 1908 vs
+  // 1898 TFLOP/s, 13 waves), so it is used from 24 waves of whole tiles on.
+  // (Mode 2, for testing, uses the machinery whenever there are whole tiles.)
+  s.dyn = p->tile_ctr != nullptr && p->tile_order != 1 &&
+          (p->tile_order == 2 ? s.dp_tiles > 0 : s.dp_tiles >= 24 * s.units);
   s.grid = static_cast<int>(s.units * vi.ctas);
   return s;
 }
@@ -440,6 +457,7 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   args.sk_iters = sch.sk_iters;
   args.sk_ws = p->sk_ws;
   args.sk_count = p->sk_count;
+  args.tile_ctr = sch.dyn ? p->tile_ctr : nullptr;
 
   const bool f32 = acc == GEMM_ACC_F32;
   cudaError_t e;
@@ -588,14 +606,15 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     const size_t ws_floats = 2ull * static_cast<size_t>(sms) * 128ull * 256ull;
     p->sk_count_words = 4ull * static_cast<size_t>(sms);
     if (cudaMalloc(&p->sk_ws, ws_floats * sizeof(float)) != cudaSuccess ||
-        cudaMalloc(&p->sk_count, p->sk_count_words * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(p->sk_count, 0, p->sk_count_words * sizeof(uint32_t)) != cudaSuccess) {
+        cudaMalloc(&p->sk_count, (p->sk_count_words + 2) * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->sk_count, 0, (p->sk_count_words + 2) * sizeof(uint32_t)) != cudaSuccess) {
       if (p->sk_ws) cudaFree(p->sk_ws);
       if (p->sk_count) cudaFree(p->sk_count);
       cudaFree(p->d_err);
       delete p;
       return GEMM_ERR_OOM;
     }
+    p->tile_ctr = p->sk_count + p->sk_count_words;
   }
   *out = p;
   return GEMM_OK;
@@ -645,6 +664,12 @@ int32_t gemm_plan_describe(gemm_plan_t p, int64_t M, int64_t N, int64_t K, gemm_
   out[4] = s.sk_units;
   out[5] = s.sk_iters;
   return 0;
+}
+
+gemm_status_t gemm_plan_set_tile_order(gemm_plan_t p, int32_t mode) {
+  if (!p || mode < 0 || mode > 2) return GEMM_ERR_INVALID_ARG;
+  p->tile_order = mode;
+  return GEMM_OK;
 }
 
 gemm_status_t gemm_plan_set_pdl(gemm_plan_t p, int32_t enable) {
@@ -730,9 +755,10 @@ gemm_status_t gemm_plan_check_error(gemm_plan_t p) {
   if (rec[0] == 0) return GEMM_OK;
   std::memcpy(p->last_err, rec, sizeof(rec));
   if (cudaMemset(p->d_err, 0, sizeof(rec)) != cudaSuccess) return GEMM_ERR_CUDA;
-  // A launch that gave up may have left stream-K counters mid-count.
+  // A launch that gave up may have left the stream-K and tile-order
+  // counters mid-count.
   if (p->sk_count &&
-      cudaMemset(p->sk_count, 0, p->sk_count_words * sizeof(uint32_t)) != cudaSuccess)
+      cudaMemset(p->sk_count, 0, (p->sk_count_words + 2) * sizeof(uint32_t)) != cudaSuccess)
     return GEMM_ERR_CUDA;
   return static_cast<gemm_status_t>(rec[0]);
 }
@@ -991,6 +1017,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   args.sk_iters = 0;
   args.sk_ws = nullptr;
   args.sk_count = nullptr;
+  args.tile_ctr = nullptr;  // static tile order: no counters here
   args.C = static_cast<uint16_t*>(C);
   args.ldc = N;
   args.a_mn = 0;

@@ -64,6 +64,8 @@ enum WaitSite : uint32_t {
   kSiteTmemFull = 4,   // epilogue waiting for a finished accumulator
   kSiteMmaDone = 5,    // teardown: waiting for the last MMAs
   kSiteDrain = 6,      // teardown: producer waiting for its last stages
+  kSiteTileFull = 7,   // a role waiting for the next tile from the tile scheduler
+  kSiteTileEmpty = 8,  // the tile scheduler waiting for a free slot of its ring
 };
 
 constexpr uint32_t kStatusTimeout = 5;  // == GEMM_ERR_TIMEOUT
@@ -90,133 +92,9 @@ struct GemmArgs {
   uint32_t* sk_count;   // per tail tile and CTA of the tile: contributions so far (self-resetting)
   uint16_t* C;          // output (fp16 bits), row pitch ldc elements: the swapped-roles
   int64_t ldc;          // epilogue stores directly
-};
-
-// One piece of work for a unit: k-blocks [kb0, kb1) of one output tile.
-struct WorkItem {
-  int32_t tile;        // linear tile index, before rastering
-  int32_t kb0, kb1;
-  int32_t sk_tile;     // index in the stream-K tail, -1 for a whole tile
-  int32_t splits;      // units contributing to this tile (1: no fix-up)
-  int32_t first_unit;  // first contributing unit (stream-K tail only)
-};
-
-// The work list of one unit, identical in every role of the unit's CTAs:
-// first its share of the stream-K tail, then its whole tiles.
-struct Sched {
-  int32_t unit, units, dp_tiles, num_kb, sk_units;
-  int64_t sk_iters;
-  int32_t next_dp;
-  int64_t x, x_end;  // this unit's remaining range of tail k-blocks
-
-  __device__ __forceinline__ Sched(const GemmArgs& a, int32_t unit_, int32_t units_)
-      : unit(unit_), units(units_), dp_tiles(a.dp_tiles), num_kb(a.num_kb),
-        sk_units(a.sk_units), sk_iters(a.sk_iters), next_dp(unit_), x(0), x_end(0) {
-    if (sk_units > 0 && unit < sk_units) {
-      x = bound(unit);
-      x_end = bound(unit + 1);
-    }
-  }
-  // First tail k-block of unit u.
-  __device__ __forceinline__ int64_t bound(int64_t u) const { return u * sk_iters / sk_units; }
-  // The unit whose range holds tail k-block `it` (the largest u with bound(u) <= it).
-  __device__ __forceinline__ int32_t unit_of(int64_t it) const {
-    return static_cast<int32_t>(((it + 1) * sk_units - 1) / sk_iters);
-  }
-  // Workspace slot unit u uses for tail tile t: 0 if t is the first tile its
-  // range touches, else 1 (only a range's first and last tiles can be partial).
-  __device__ __forceinline__ int32_t slot_of(int32_t u, int32_t t) const {
-    return static_cast<int32_t>(bound(u) / num_kb) == t ? 0 : 1;
-  }
-  // Stream-K pieces come first and whole tiles after them: the fix-up of a
-  // shared tile (reading the other units' partials) then overlaps the main
-  // loop of a later whole tile instead of ending the kernel.
-  __device__ __forceinline__ bool next(WorkItem& w) {
-    if (x >= x_end && next_dp < dp_tiles) {
-      w.tile = next_dp;
-      w.kb0 = 0;
-      w.kb1 = num_kb;
-      w.sk_tile = -1;
-      w.splits = 1;
-      w.first_unit = unit;
-      next_dp += units;
-      return true;
-    }
-    if (x < x_end) {
-      const int32_t t = static_cast<int32_t>(x / num_kb);
-      const int64_t t0 = static_cast<int64_t>(t) * num_kb, t1 = t0 + num_kb;
-      const int64_t e = x_end < t1 ? x_end : t1;
-      w.tile = dp_tiles + t;
-      w.kb0 = static_cast<int32_t>(x - t0);
-      w.kb1 = static_cast<int32_t>(e - t0);
-      w.sk_tile = t;
-      w.first_unit = unit_of(t0);
-      w.splits = unit_of(t1 - 1) - w.first_unit + 1;
-      x = e;
-      return true;
-    }
-    return false;
-  }
-};
-
-// Tile configuration.  kCtas CTAs cooperate on one tile of kTileM x kBN.
-template <int kCtas_, int kStages_, bool kAccF16_, int kBN_ = 256, bool kSwap_ = false,
-          int kMc_ = 1>
-struct GemmCfg {
-  static constexpr int kCtas = kCtas_;
-  // kMc = 2: a cluster holds two CTA pairs working on neighbouring tiles of
-  // the same tile-row; the pairs share the tile-row's A block, each CTA
-  // loading half of its 128 rows and multicasting it to the CTA in the same
-  // position of the other pair, so every SM requests half as many A bytes.
-  static constexpr int kMc = kMc_;
-  static constexpr int kClusterCtas = kCtas * kMc;
-  // Swapped roles (for small M): the MMA's "A" operand is a 128-row tile of B
-  // and its "B" operand a kBN-row tile of A, so D = tile of C^T.
-  static constexpr bool kSwap = kSwap_;
-  static constexpr int kBM = 128;                 // rows of C per CTA
-  static constexpr int kBN = kBN_;                // columns of C per tile
-  static constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle row)
-  static constexpr int kTileM = kBM * kCtas;      // rows of C per tile
-  static constexpr int kBRows = kBN / kCtas;      // rows of B each CTA loads
-  static constexpr int kStages = kStages_;
-  static constexpr bool kAccF16 = kAccF16_;
-  static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = kBRows * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;  // landed in each CTA per stage
-  static constexpr int kTxBytes = kStageBytes * kCtas;   // counted on the leader's barrier
-  static constexpr int kEpiWarps = 4;
-  static constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 fp16, 128B swizzle
-  static constexpr int kEpiBytes = kSwap ? 0 : kEpiWarps * 2 * kEpiBufBytes;
-  static constexpr int kOffA = 0;
-  static constexpr int kOffB = kStages * kABytes;
-  static constexpr int kOffEpi = kStages * kStageBytes;
-  static constexpr int kOffBar = kOffEpi + kEpiBytes;
-  static constexpr int kNumBars = 2 * kStages + 5;  // full, empty, tmem_full[2], tmem_empty[2], mma_done
-  static constexpr int kOffSlot = kOffBar + kNumBars * 8;
-  static constexpr int kOffAbort = kOffSlot + 4;
-  static constexpr int kOffFlag = kOffAbort + 4;           // stream-K "last contributor" flag
-  static constexpr int kSmemBytes = kOffFlag + 4 + 1024;   // + slack to align the base to 1024
-  static constexpr int kPartialFloats = kBM * kBN;         // one CTA's share of a partial tile
-  static constexpr int kTmemCols = 2 * kBN;
-  static constexpr int kWarpProducerB = 6;  // warps 0 and 6 load A and B
-  static constexpr int kThreads = 224;
-  static constexpr uint32_t kIdesc = ptx::idesc_f16(kTileM, kBN, !kAccF16);
-
-  static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair");
-  static_assert(kMc == 1 || (kMc == 2 && kCtas == 2 && !kSwap),
-                "A multicast between two CTA pairs only");
-  static_assert(kSwap ? (kCtas == 1 && (kBN == 16 || kBN == 32 || kBN == 64))
-                      : (kBN == 64 || kBN == 128 || kBN == 256),
-                "tile width: 64, 128 or 256; 16, 32 or 64 with swapped roles (one CTA)");
-  static_assert(kBRows >= 8 && kBRows % 8 == 0, "B rows per CTA: whole 8-row swizzle atoms");
-  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
-                "TMEM is allocated in powers of two from 32 to 512 columns");
-  static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory per CTA");
-  static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1024 B alignment");
-  // Barriers sit after every TMA destination, never inside one (tilus "A
-  // Minimal Hopper Matmul", Epilogue note: a barrier placed inside a live TMA
-  // destination is silently corrupted).
-  static_assert(kOffBar >= kOffEpi + kEpiBytes, "barriers overlap a TMA buffer");
+  // Dynamic order of whole tiles: [0] tickets taken, [1] units finished (both
+  // back to zero when a launch ends).  nullptr: the static round robin.
+  uint32_t* tile_ctr;
 };
 
 struct Watch {
@@ -269,6 +147,198 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
   return __all_sync(0xffffffffu, wait_bar<kClusterScope>(bar, parity, w, site, tile, honor_abort));
 }
 
+// One piece of work for a unit: k-blocks [kb0, kb1) of one output tile.
+struct WorkItem {
+  int32_t tile;        // linear tile index, before rastering
+  int32_t kb0, kb1;
+  int32_t sk_tile;     // index in the stream-K tail, -1 for a whole tile
+  int32_t splits;      // units contributing to this tile (1: no fix-up)
+  int32_t first_unit;  // first contributing unit (stream-K tail only)
+};
+
+// Where a role reads the dynamic tile order: a two-slot ring in its own
+// CTA's shared memory, filled by the unit's tile scheduler (tile_full[i]
+// completes when slot i holds the next tile), and emptied by arriving on
+// tile_empty[i] in the leader CTA of the cluster.  Every consumer warp reads
+// every slot, in order.
+struct TileRing {
+  uint32_t slot0;   // this CTA: slot i at slot0 + 4 i
+  uint32_t full0;   // this CTA: tile_full[i] at full0 + 8 i
+  uint32_t empty0;  // the cluster's leader CTA: tile_empty[i] at empty0 + 8 i
+  Watch w;
+  bool cluster;     // the kernel runs in clusters (addresses are cluster-wide)
+  uint32_t took;    // nonzero for the leader's A producer: it arrives here on each read,
+                    // which tells the scheduler to take the next ticket
+};
+
+// The work list of one unit, identical in every role of the unit's CTAs:
+// first its share of the stream-K tail, then its whole tiles.  Whole tiles
+// come round robin (tile unit, unit + units, ...) in the static order; in
+// the dynamic order (tile_ctr set) the first is still tile `unit` and the
+// rest are the tiles the unit's scheduler takes from a global ticket
+// counter as the unit needs them, so tiles start in order across units and
+// the tiles in flight stay within about one wave however far units drift
+// apart (operands then stay in L2 between their uses by neighbouring tiles).
+struct Sched {
+  int32_t unit, units, dp_tiles, num_kb, sk_units;
+  int64_t sk_iters;
+  int32_t next_dp;
+  int64_t x, x_end;  // this unit's remaining range of tail k-blocks
+  bool dyn;          // dynamic order of whole tiles after the first
+  bool first_done;   // the unit's first whole tile has been handed out
+  int32_t n;         // ring slots read so far
+  TileRing ring;
+
+  __device__ __forceinline__ Sched(const GemmArgs& a, int32_t unit_, int32_t units_,
+                                   const TileRing& ring_ = TileRing{})
+      : unit(unit_), units(units_), dp_tiles(a.dp_tiles), num_kb(a.num_kb),
+        sk_units(a.sk_units), sk_iters(a.sk_iters), next_dp(unit_), x(0), x_end(0),
+        dyn(a.tile_ctr != nullptr), first_done(false), n(0), ring(ring_) {
+    if (sk_units > 0 && unit < sk_units) {
+      x = bound(unit);
+      x_end = bound(unit + 1);
+    }
+  }
+  // The next tile from the scheduler's ring, or -1 when there are no more
+  // (or the wait gave up).  Called by whole, converged warps; lane 0 frees
+  // the slot, once the slot's value has been read.
+  __device__ __forceinline__ int32_t ring_read() {
+    const int i = n & 1;
+    const uint32_t par = static_cast<uint32_t>((n >> 1) & 1);
+    ++n;
+    const bool ok =
+        ring.cluster ? wait_bar_warp<true>(ring.full0 + 8u * i, par, ring.w, kSiteTileFull, -1)
+                     : wait_bar_warp<false>(ring.full0 + 8u * i, par, ring.w, kSiteTileFull, -1);
+    const uint32_t v = ok ? ptx::ld_shared_u32(ring.slot0 + 4u * i) : 0xffffffffu;
+    if ((threadIdx.x & 31) == 0) {
+      if (ring.cluster)
+        ptx::mbar_arrive_relaxed_cluster_after(ring.empty0 + 8u * i, v);
+      else
+        ptx::mbar_arrive_relaxed_cta_after(ring.empty0 + 8u * i, v);
+      if (ring.took) ptx::mbar_arrive_relaxed_cta_after(ring.took, v);
+    }
+    return static_cast<int32_t>(v);
+  }
+  __device__ __forceinline__ void whole(WorkItem& w, int32_t t) const {
+    w.tile = t;
+    w.kb0 = 0;
+    w.kb1 = num_kb;
+    w.sk_tile = -1;
+    w.splits = 1;
+    w.first_unit = unit;
+  }
+  // First tail k-block of unit u.
+  __device__ __forceinline__ int64_t bound(int64_t u) const { return u * sk_iters / sk_units; }
+  // The unit whose range holds tail k-block `it` (the largest u with bound(u) <= it).
+  __device__ __forceinline__ int32_t unit_of(int64_t it) const {
+    return static_cast<int32_t>(((it + 1) * sk_units - 1) / sk_iters);
+  }
+  // Workspace slot unit u uses for tail tile t: 0 if t is the first tile its
+  // range touches, else 1 (only a range's first and last tiles can be partial).
+  __device__ __forceinline__ int32_t slot_of(int32_t u, int32_t t) const {
+    return static_cast<int32_t>(bound(u) / num_kb) == t ? 0 : 1;
+  }
+  // Stream-K pieces come first and whole tiles after them: the fix-up of a
+  // shared tile (reading the other units' partials) then overlaps the main
+  // loop of a later whole tile instead of ending the kernel.
+  __device__ __forceinline__ bool next(WorkItem& w) {
+    if (x >= x_end) {
+      if (dyn && first_done) {
+        const int32_t t = ring_read();
+        if (t < 0) return false;
+        whole(w, t);
+        return true;
+      }
+      first_done = true;
+      if (next_dp >= dp_tiles) return false;
+      whole(w, next_dp);
+      next_dp += units;
+      return true;
+    }
+    if (x < x_end) {
+      const int32_t t = static_cast<int32_t>(x / num_kb);
+      const int64_t t0 = static_cast<int64_t>(t) * num_kb, t1 = t0 + num_kb;
+      const int64_t e = x_end < t1 ? x_end : t1;
+      w.tile = dp_tiles + t;
+      w.kb0 = static_cast<int32_t>(x - t0);
+      w.kb1 = static_cast<int32_t>(e - t0);
+      w.sk_tile = t;
+      w.first_unit = unit_of(t0);
+      w.splits = unit_of(t1 - 1) - w.first_unit + 1;
+      x = e;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Tile configuration.  kCtas CTAs cooperate on one tile of kTileM x kBN.
+template <int kCtas_, int kStages_, bool kAccF16_, int kBN_ = 256, bool kSwap_ = false,
+          int kMc_ = 1>
+struct GemmCfg {
+  static constexpr int kCtas = kCtas_;
+  // kMc = 2: a cluster holds two CTA pairs working on neighbouring tiles of
+  // the same tile-row; the pairs share the tile-row's A block, each CTA
+  // loading half of its 128 rows and multicasting it to the CTA in the same
+  // position of the other pair, so every SM requests half as many A bytes.
+  static constexpr int kMc = kMc_;
+  static constexpr int kClusterCtas = kCtas * kMc;
+  // Swapped roles (for small M): the MMA's "A" operand is a 128-row tile of B
+  // and its "B" operand a kBN-row tile of A, so D = tile of C^T.
+  static constexpr bool kSwap = kSwap_;
+  static constexpr int kBM = 128;                 // rows of C per CTA
+  static constexpr int kBN = kBN_;                // columns of C per tile
+  static constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle row)
+  static constexpr int kTileM = kBM * kCtas;      // rows of C per tile
+  static constexpr int kBRows = kBN / kCtas;      // rows of B each CTA loads
+  static constexpr int kStages = kStages_;
+  static constexpr bool kAccF16 = kAccF16_;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = kBRows * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;  // landed in each CTA per stage
+  static constexpr int kTxBytes = kStageBytes * kCtas;   // counted on the leader's barrier
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 fp16, 128B swizzle
+  static constexpr int kEpiBytes = kSwap ? 0 : kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kStages * kABytes;
+  static constexpr int kOffEpi = kStages * kStageBytes;
+  static constexpr int kOffBar = kOffEpi + kEpiBytes;
+  // full, empty, tmem_full[2], tmem_empty[2], mma_done, tile_full[2], tile_empty[2],
+  // tile_took
+  static constexpr int kNumBars = 2 * kStages + 10;
+  static constexpr int kOffSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffSlot + 4;
+  static constexpr int kOffFlag = kOffAbort + 4;           // stream-K "last contributor" flag
+  static constexpr int kOffTiles = kOffFlag + 4;           // tile ring: two slots
+  static constexpr int kSmemBytes = kOffTiles + 8 + 1024;  // + slack to align the base to 1024
+  static constexpr int kPartialFloats = kBM * kBN;         // one CTA's share of a partial tile
+  static constexpr int kTmemCols = 2 * kBN;
+  static constexpr int kWarpProducerB = 6;  // warps 0 and 6 load A and B
+  static constexpr int kWarpSched = 7;      // tile scheduler (dynamic order, leader CTA)
+  static constexpr int kThreads = 256;
+  // Warps that read the tile ring: in every CTA both producers and the four
+  // epilogue warps, and the MMA issuer in each pair's (or lone CTA's) leader.
+  static constexpr int kTileConsumers = kClusterCtas * (2 + kEpiWarps) + (kCtas == 1 ? 1 : kMc);
+  static constexpr uint32_t kIdesc = ptx::idesc_f16(kTileM, kBN, !kAccF16);
+
+  static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair");
+  static_assert(kMc == 1 || (kMc == 2 && kCtas == 2 && !kSwap),
+                "A multicast between two CTA pairs only");
+  static_assert(kSwap ? (kCtas == 1 && (kBN == 16 || kBN == 32 || kBN == 64))
+                      : (kBN == 64 || kBN == 128 || kBN == 256),
+                "tile width: 64, 128 or 256; 16, 32 or 64 with swapped roles (one CTA)");
+  static_assert(kBRows >= 8 && kBRows % 8 == 0, "B rows per CTA: whole 8-row swizzle atoms");
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
+                "TMEM is allocated in powers of two from 32 to 512 columns");
+  static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory per CTA");
+  static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1024 B alignment");
+  // Barriers sit after every TMA destination, never inside one (tilus "A
+  // Minimal Hopper Matmul", Epilogue note: a barrier placed inside a live TMA
+  // destination is silently corrupted).
+  static_assert(kOffBar >= kOffEpi + kEpiBytes, "barriers overlap a TMA buffer");
+};
+
 // Grouped raster: tiles are walked down a group of `group` tile-rows before
 // moving one tile-column right, so tiles in flight at the same time share A
 // rows and B rows in L2.  A bijection of [0, tiles_m*tiles_n).
@@ -319,10 +389,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   auto bar_tfull = [&](int b) { return bar0 + 8u * (2 * S + b); };
   auto bar_tempty = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
   const uint32_t bar_mma_done = bar0 + 8u * (2 * S + 4);
+  auto bar_tile_full = [&](int i) { return bar0 + 8u * (2 * S + 5 + i); };
+  auto bar_tile_empty = [&](int i) { return bar0 + 8u * (2 * S + 7 + i); };
+  const uint32_t bar_tile_took = bar0 + 8u * (2 * S + 9);
   auto sA = [&](int s) { return sb + Cfg::kOffA + s * Cfg::kABytes; };
   auto sB = [&](int s) { return sb + Cfg::kOffB + s * Cfg::kBBytes; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
   const Watch w{abort_flag, args.err, args.timeout_ns};
+  // The dynamic tile order as every role reads it (tile_empty lives in the
+  // cluster's leader, rank 0, where the scheduler runs).
+  const TileRing ring{sb + Cfg::kOffTiles, bar_tile_full(0),
+                      kPair ? ptx::mapa(bar_tile_empty(0), 0) : bar_tile_empty(0), w, kPair,
+                      warp == 0 && rank == 0 ? bar_tile_took : 0u};
 
   if (threadIdx.x == 0) {
     ptx::prefetch_tmap(&tmA);
@@ -337,6 +415,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       ptx::mbar_init(bar_tempty(b), Cfg::kEpiWarps * Cfg::kCtas);
     }
     ptx::mbar_init(bar_mma_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar_tile_full(i), 1);  // the scheduler's publication
+      ptx::mbar_init(bar_tile_empty(i), Cfg::kTileConsumers);
+    }
+    ptx::mbar_init(bar_tile_took, 1);  // the leader's A producer read a tile
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -387,7 +470,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                           static_cast<int32_t>(pair) * rows
                     : tile_nb(nbx) * Cfg::kBN + static_cast<int32_t>(cta) * Cfg::kBRows;
       };
-      Sched sched(args, unit, units);
+      Sched sched(args, unit, units, ring);
       WorkItem wi;
       // The first work item is worked out before the wait for the previous
       // kernel, so that after it only the loads themselves remain.  So is an
@@ -491,7 +574,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                              (args.b_mn ? ptx::kIdescBMnMajor : 0u);
       const uint64_t a_kstep = args.a_mn ? 128u : 2u;
       const uint64_t b_kstep = args.b_mn ? 128u : 2u;
-      Sched sched(args, unit, units);
+      Sched sched(args, unit, units, ring);
       WorkItem wi;
       int stage = 0;
       uint32_t phase = 0;
@@ -560,6 +643,60 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       __syncwarp();
       wait_bar_warp<kPair>(bar_mma_done, 0u, w, kSiteMmaDone, -1, /*honor_abort=*/false);
     }
+  } else if (warp == Cfg::kWarpSched) {
+    // ----------------------------------------------------- tile scheduler --
+    // Dynamic order: the cluster's leader takes a ticket from the global
+    // counter one tile ahead of its A producer (the first ticket at once,
+    // each later one when that producer has read the tile before it, i.e.
+    // has started it), so tickets go out in the order units start tiles, and
+    // publishes the tile (or -1: none left) to the same slot of every CTA of
+    // the cluster once that slot is free (all of the cluster's consumer
+    // warps have read the slot's last tile).  The last unit to finish sets
+    // both counters back to zero for the next launch.
+    if (args.tile_ctr != nullptr && rank == 0 && unit < args.dp_tiles) {
+      ptx::griddep_wait();  // the counters are global memory
+      const int32_t active = units < args.dp_tiles ? units : args.dp_tiles;
+      bool ok = true;
+      for (int32_t n = 0;; ++n) {
+        if (n > 0 && !wait_bar_warp<false>(bar_tile_took, static_cast<uint32_t>((n - 1) & 1), w,
+                                           kSiteTileEmpty, -1)) {
+          ok = false;
+          break;
+        }
+        uint32_t ticket = 0;
+        if (lane == 0) ticket = atomicAdd(args.tile_ctr, 1u);
+        ticket = __shfl_sync(0xffffffffu, ticket, 0) + static_cast<uint32_t>(units);
+        const int32_t t =
+            ticket < static_cast<uint32_t>(args.dp_tiles) ? static_cast<int32_t>(ticket) : -1;
+        const int i = n & 1;
+        const uint32_t par = static_cast<uint32_t>(((n >> 1) & 1) ^ 1);
+        if (!wait_bar_warp<kPair>(bar_tile_empty(i), par, w, kSiteTileEmpty, t)) {
+          ok = false;
+          break;
+        }
+        if (lane < Cfg::kClusterCtas) {
+          const uint32_t slot = sb + Cfg::kOffTiles + 4u * static_cast<uint32_t>(i);
+          if constexpr (kPair) {
+            ptx::st_shared_cluster_u32(ptx::mapa(slot, static_cast<uint32_t>(lane)),
+                                       static_cast<uint32_t>(t));
+            ptx::mbar_arrive_release_cluster(
+                ptx::mapa(bar_tile_full(i), static_cast<uint32_t>(lane)));
+          } else {
+            ptx::st_shared_u32(slot, static_cast<uint32_t>(t));
+            ptx::mbar_arrive(bar_tile_full(i));
+          }
+        }
+        __syncwarp();
+        if (t < 0) break;
+      }
+      if (ok && lane == 0) {
+        __threadfence();  // this unit's tickets are taken before it counts itself done
+        if (atomicAdd(args.tile_ctr + 1, 1u) == static_cast<uint32_t>(active - 1)) {
+          args.tile_ctr[0] = 0u;
+          args.tile_ctr[1] = 0u;
+        }
+      }
+    }
   } else if constexpr (Cfg::kSwap) {
     // ---------------------------------------------- epilogue, swapped roles --
     ptx::griddep_wait();  // writes C and the workspace
@@ -574,10 +711,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     auto partial = [&](int32_t u, int32_t slot) {
       return args.sk_ws + static_cast<size_t>(u * 2 + slot) * static_cast<size_t>(Cfg::kPartialFloats);
     };
-    Sched sched(args, unit, units);
+    Sched sched(args, unit, units, ring);
     WorkItem wi;
     int32_t acc_iter = 0;
-    while (sched.next(wi)) {
+    // All epilogue warps take the same decision (a failed wait for the next
+    // tile ends the loop in every warp, none is left at a barrier below).
+    while (ptx::named_barrier_and(1, 32 * Cfg::kEpiWarps, sched.next(wi))) {
       int32_t mb, nb;
       raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nb);
       const int buf = acc_iter & 1;
@@ -692,11 +831,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       return args.sk_ws + (static_cast<size_t>(u * 2 + slot) * Cfg::kClusterCtas + rank) *
                               static_cast<size_t>(Cfg::kPartialFloats);
     };
-    Sched sched(args, unit, units);
+    Sched sched(args, unit, units, ring);
     WorkItem wi;
     uint32_t stores = 0;
     int32_t acc_iter = 0;
-    while (sched.next(wi)) {
+    // All epilogue warps take the same decision (a failed wait for the next
+    // tile ends the loop in every warp, none is left at a barrier below).
+    while (ptx::named_barrier_and(1, 32 * Cfg::kEpiWarps, sched.next(wi))) {
       int32_t mb, nbx;
       raster(wi.tile, args.tiles_m, args.tiles_n, args.group_m, mb, nbx);
       const int32_t nb = tile_nb(nbx);

@@ -53,6 +53,46 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Arrive on a barrier of any CTA in the cluster with release semantics at
+// cluster scope: this thread's earlier writes to that CTA's shared memory
+// are visible to whoever sees the phase complete.  For a thread with no bulk
+// copies in flight (the tile scheduler), where it is cheap.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
+// Relaxed arrive on a barrier of any CTA in the cluster, issued only once
+// `after` is available: a value this thread loaded is fully read before the
+// arrival can be seen.
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster_after(uint32_t cluster_bar,
+                                                                   uint32_t after) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar),
+               "r"(after)
+               : "memory");
+}
+
+// The same on a barrier of this CTA.
+__device__ __forceinline__ void mbar_arrive_relaxed_cta_after(uint32_t bar, uint32_t after) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar), "r"(after)
+               : "memory");
+}
+
+// 32-bit store to shared memory of any CTA in the cluster (address from mapa).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // True once the phase with parity `parity` has completed.  On a fresh barrier
 // (current phase 0 in progress) parity 1 counts as completed, which is what
 // lets a producer's first pass through an empty ring go straight through.

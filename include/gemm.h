@@ -160,6 +160,17 @@ GEMM_API gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout
  * stay deterministic); fp16 accumulation always uses whole tiles. */
 GEMM_API gemm_status_t gemm_plan_set_schedule(gemm_plan_t plan, int32_t mode);
 
+/* Order of whole tiles (a work-scheduling detail; results never depend on
+ * it): 0 = automatic (default: dynamic from 24 waves of whole tiles on,
+ * e.g. 16384^3), 1 = static round robin over the persistent units, 2 =
+ * dynamic whenever there are whole tiles (testing).  In the dynamic order
+ * each unit's first whole tile is fixed and the rest are taken from a
+ * global ticket counter in the plan as the unit needs them, so tiles start
+ * in order across units and the tiles in flight stay within about one wave
+ * (their shared operands stay in L2).  GEMM_ERR_INVALID_ARG for other
+ * values.  No counterpart in the source pages (a scheduling detail). */
+GEMM_API gemm_status_t gemm_plan_set_tile_order(gemm_plan_t plan, int32_t mode);
+
 /* Programmatic dependent launch (default 1 = on): the GEMM kernel is launched
  * so that its set-up (barriers, tensor-memory allocation) may overlap the end
  * of the previous kernel in the stream; it waits for that kernel to complete
