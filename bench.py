@@ -54,6 +54,8 @@ def parse():
                    help="storage of A and B: k = K-contiguous, m/n = M/N-contiguous")
     p.add_argument("--acc", default="f32", choices=["f32", "f16"])
     p.add_argument("--variant", default=None, help="force a kernel variant by name")
+    p.add_argument("--tile-order", default="auto", choices=["auto", "static", "dynamic"],
+                   help="order of whole tiles over the persistent units (results do not depend on it)")
     p.add_argument("--graph", action="store_true",
                    help="capture the K timed launches in one CUDA graph (GPU time without "
                         "per-call host overhead; for small shapes)")
@@ -255,6 +257,7 @@ def run_ours(args):
     plan = g.Plan(local)
     if args.variant:
         plan.set_variant(args.variant)
+    plan.set_tile_order(args.tile_order)
     w_full = resolve_workload(args)
     w = w_full
     a_np, b_np = wl.inputs_for(w_full)

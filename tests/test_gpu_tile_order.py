@@ -140,6 +140,32 @@ def test_timeout_in_dynamic_order_leaves_a_usable_plan():
     pd.close()
 
 
+def test_graph_replay_in_dynamic_order():
+    """A captured launch in the dynamic order replays correctly: the ticket
+    counters are back at zero at the end of every launch, graph or not."""
+    M, N, K = 4096, 4096, 256
+    a, b = wl.draw(M, N, K, seed=80)
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    ps, pd = _plan(order="static"), _plan(order="dynamic")
+    ref = _run(ps, ta, tb, M, N)[0]
+    c = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pd.run(ta, tb, c)               # first call outside the capture
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        pd.run(ta, tb, c)
+    for _ in range(4):
+        c.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(c, ref)
+    pd.check_error()
+    ps.close()
+    pd.close()
+
+
 def test_set_tile_order_rejects_other_values(plan):
     with pytest.raises(g.GemmError):
         plan.set_tile_order(3)
