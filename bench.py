@@ -56,6 +56,10 @@ def parse():
     p.add_argument("--variant", default=None, help="force a kernel variant by name")
     p.add_argument("--tile-order", default="auto", choices=["auto", "static", "dynamic"],
                    help="order of whole tiles over the persistent units (results do not depend on it)")
+    p.add_argument("--schedule", default="auto", choices=["auto", "whole", "streamk"],
+                   help="work schedule: automatic, whole tiles only, or a stream-K share whenever possible")
+    p.add_argument("--pdl", default="on", choices=["on", "off"],
+                   help="programmatic dependent launch of consecutive GEMMs")
     p.add_argument("--graph", action="store_true",
                    help="capture the K timed launches in one CUDA graph (GPU time without "
                         "per-call host overhead; for small shapes)")
@@ -258,6 +262,8 @@ def run_ours(args):
     if args.variant:
         plan.set_variant(args.variant)
     plan.set_tile_order(args.tile_order)
+    plan.set_schedule(args.schedule)
+    plan.set_pdl(args.pdl == "on")
     w_full = resolve_workload(args)
     w = w_full
     a_np, b_np = wl.inputs_for(w_full)
@@ -382,8 +388,11 @@ def run_ours(args):
         rate, used, sample, _ = cpu_oracle_rate(w, args.cpu_rows, steps=1, a=a_np, b=b_np)
         cpu = {"value": rate, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample}
 
+    # The recorded ncu traffic is for the automatic settings only.
+    defaults = (args.layout == "kk" and args.schedule == "auto" and args.tile_order == "auto"
+                and args.pdl == "on")
     traffic = (_recorded_traffic(w.name, args.acc, plan.pick_variant(w.M, w.N, w.K, args.acc)[0])
-               if args.layout == "kk" else None)
+               if defaults else None)
     variant, grid = plan.pick_variant(w.M, w.N, w.K, args.acc)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -395,7 +404,8 @@ def run_ours(args):
                    "l2": l2_note,
                    "parallelism": (f"M split x{world}" if strong else f"replicas x{world}")
                                   if world > 1 else "single GPU",
-                   "launch": "CUDA graph of the K steps" if graph is not None else "one call per step"},
+                   "launch": "CUDA graph of the K steps" if graph is not None else "one call per step",
+                   "schedule": args.schedule, "tile_order": args.tile_order, "pdl": args.pdl},
         "pct_of_peak": value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
