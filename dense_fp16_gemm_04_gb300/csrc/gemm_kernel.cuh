@@ -3,7 +3,7 @@
 //   C[M,N] = A[M,K] x B[N,K]^T, fp16 in, fp32 or fp16 accumulate, fp16 out
 //   (tilus "A Minimal Hopper Matmul", section "Block Tiling").
 //
-// One template, three forms:
+// One template, four forms:
 //   kCtas = 1           one CTA per SM owns a 128 x kBN tile of C (kBN = 64..256);
 //   kCtas = 2           a cluster of two CTAs on neighbouring SMs owns a
 //                       256 x kBN tile: each CTA loads its 128 rows of A and
@@ -11,6 +11,11 @@
 //                       leader CTA issues tcgen05.mma.cta_group::2 (M = 256)
 //                       over both CTAs' shared memory, so every SM stages a
 //                       third less operand data per FLOP (at kBN = 256);
+//   kCtas = 2, kMc = 2  a cluster of four CTAs: two such pairs on neighbouring
+//                       tiles of one tile-row, each CTA loading half of its
+//                       pair's A rows and multicasting them into both pairs
+//                       (for rows whose pitch is not a multiple of 128 bytes,
+//                       where every TMA row straddles two L2 lines);
 //   kSwap               roles swapped for C with few rows: the MMA's M runs
 //                       over 128 columns of C (rows of B) and its N over
 //                       kBN = 16..64 rows of C, and the epilogue writes the
@@ -18,13 +23,15 @@
 // Operands are K-contiguous or M/N-contiguous (run-time choice: TMA box shape,
 // shared-memory descriptor and the instruction descriptor's transpose bits).
 //
-// Units (CTAs or pairs) are persistent.  Their work list (Sched) is a share of
-// the part-empty last wave's tiles cut into equal k-block ranges (stream-K)
-// followed by whole tiles dealt round robin over a grouped raster.  A tile
-// shared by several units is finished by whichever contributes last: the
-// others park fp32 partials in a workspace, and the last one sums them in
-// unit order.  Inside a CTA the work is split by warp, after the producer /
-// consumer split of tilus "Warp Specialization", redesigned for tcgen05:
+// Units (CTAs, pairs or four-CTA clusters) are persistent.  Their work list
+// (Sched) is a share of the part-empty last wave's tiles cut into equal
+// k-block ranges (stream-K) followed by whole tiles over a grouped raster,
+// dealt round robin or, for long runs of waves, in a dynamic order taken
+// from a global ticket counter.  A tile shared by several units is finished
+// by whichever contributes last: the others park fp32 partials in a
+// workspace, and the last one sums them in unit order.  Inside a CTA the work
+// is split by warp, after the producer / consumer split of tilus "Warp
+// Specialization", redesigned for tcgen05:
 //
 //   warps 0 and 6    TMA producers: a kStages-deep ring of k-blocks, warp 0
 //                    loading A and warp 6 loading B.
@@ -38,6 +45,8 @@
 // converged form keeps it fed.
 //   warps 2..5       epilogue: tcgen05.ld the accumulator, round to fp16,
 //                    stage through swizzled shared memory, TMA-store.
+//   warp 7           tile scheduler of the dynamic order (cluster leader only;
+//                    idle otherwise).
 //
 // The accumulator is double-buffered in TMEM (2 x kBN columns), so the
 // epilogue of one work item overlaps the main loop of the next; tmem_full /
