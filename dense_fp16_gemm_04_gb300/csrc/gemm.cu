@@ -246,8 +246,9 @@ struct Schedule {
 // K-contiguous rows whose pitch is not a multiple of 128 bytes (K % 64 != 0)
 // make every 128-byte TMA row straddle two L2 lines, doubling the load
 // requests each SM issues; there two pairs share A by multicast, halving A's
-// requests (3000 x 5000 x 4104: 1514 vs 1311 TFLOP/s).  On aligned rows the
-// fewer resident units cost more than the multicast saves (8192^3: -6%).
+// requests (3000 x 5000 x 4104: 1514 vs 1311 TFLOP/s).  On aligned rows it
+// ties with the one-pair kernel when the clock is not capped (8192^3: 1884 vs
+// 1871) and lost 6% once power-capped, with 144 of the 152 SMs in use.
 int auto_variant(int64_t M, int64_t N, int64_t K, bool k_major, int max_pairs, int max_quads) {
   if (M <= 16) return kVariantSwap16;
   if (M <= 32) return kVariantSwap32;
