@@ -387,14 +387,20 @@ def run_ours(args):
         e_steps = max(3, min(args.steps, 10))
         barrier()
         t0 = time.perf_counter()
+        marks = []
         for _ in range(e_steps):
-            plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)
-        dt = reduce_max(time.perf_counter() - t0, world, dev)
+            plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)  # synchronous
+            marks.append(time.perf_counter())
+        dt = reduce_max(marks[-1] - t0, world, dev)
+        step_ms = sorted((b - a) * 1e3 for a, b in zip([t0] + marks[:-1], marks))
         e2e = {"value": (aggregate_tflops(1, e_steps, float(w_full.flops), dt) if strong
                          else aggregate_tflops(world, e_steps, flops, dt)), "unit": UNIT,
                "h2d_bytes_per_step": int(a_np.nbytes + b_np.nbytes),
                "d2h_bytes_per_step": int(w.M * w.N * 2),
-               "ms_per_step": dt / e_steps * 1e3, "steps": e_steps}
+               "ms_per_step": dt / e_steps * 1e3, "steps": e_steps,
+               # this rank's steps one by one: a host-link hiccup shows here
+               "step_ms": {"min": step_ms[0], "median": step_ms[len(step_ms) // 2],
+                           "max": step_ms[-1]}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
