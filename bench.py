@@ -95,9 +95,12 @@ class ClockSampler:
     (read-only queries) on a background thread while the timed region runs.
     If NVML cannot be loaded the clocks are reported as unavailable."""
 
-    # NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
-    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    # NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*); any other
+    # bit except GPU idle (0x1) is reported by its value.
+    REASONS = {0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    IDLE = 0x1
 
     def __init__(self, torch_device, period_s: float = 0.002):
         self.period = period_s
@@ -168,8 +171,13 @@ class ClockSampler:
             for bit, name in self.REASONS.items():
                 if mask & bit:
                     reasons.add(name)
+            other = mask & ~(self.IDLE | sum(self.REASONS))
+            if other:
+                reasons.add("0x%x" % other)
         power = [x[1] for x in self.samples if x[1] is not None]
-        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+        ranked = sorted(sm)
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": ranked[0],
+                "sm_p10_mhz": ranked[len(ranked) // 10],
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
                 "samples": len(sm), "power_w_max": max(power) if power else None,
                 "source": "nvml, polled every %.0f ms in the timed region" % (self.period * 1e3)}

@@ -118,3 +118,21 @@ def test_two_gloo_ranks_split_rows_disjointly():
         p.join(120)
         assert p.exitcode == 0
     assert out[0] and out[1]
+
+
+def test_clock_summary_names_every_reason():
+    """The clock record lists every clock-event reason seen (GPU idle aside),
+    unnamed bits by value, with the minimum and 10th-percentile SM clock."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    s = bench.ClockSampler(torch.device("cpu"))
+    s.samples = ([(2070.0, 300.0, 0x0)] * 16 + [(1320.0, 360.0, 0x4 | 0x10)] * 3 +
+                 [(2070.0, 100.0, 0x1 | 0x400)])
+    d = s.summary()
+    assert d["reasons"] == ["0x400", "sw_power_cap", "sync_boost"]
+    assert d["sm_mhz"] == 2070.0 and d["sm_min_mhz"] == 1320.0
+    assert d["sm_p10_mhz"] == 1320.0
+    assert d["samples"] == 20 and d["power_w_max"] == 360.0
+    s.samples = [(2070.0, 300.0, 0x1)] * 5
+    assert s.summary()["reasons"] == []
