@@ -78,3 +78,33 @@ def test_partition_properties():
             first = unit_of(tt * KB, iters, usk)
             last = unit_of(tt * KB + KB - 1, iters, usk)
             assert owners == set(range(first, last + 1))
+
+
+def test_whole_pieces_of_few_tall_tiles():
+    """Fewer tiles than units (the swapped-roles kernels on C with few rows):
+    every tile is cut into the same whole number of k-pieces, T * floor(U / T)
+    units with at least 16 k-blocks each.  Then each unit holds exactly one
+    piece of one tile, each tile has exactly `pieces` contributors, and the
+    pieces of a tile are consecutive units."""
+    rng = random.Random(1)
+    cases = [(64, 128, 152), (128, 256, 152), (96, 128, 152), (32, 64, 152), (64, 33, 152)]
+    cases += [(rng.randint(1, 151), rng.randint(16, 400), 152) for _ in range(300)]
+    for T, KB, U in cases:
+        pieces = min(U // T, KB // 16)
+        if pieces < 2:
+            continue
+        usk = T * pieces
+        iters = T * KB
+        seen = {}
+        for u in range(usk):
+            items = work(u, usk, T, KB, 0, usk)
+            assert len(items) == 1, (T, KB, U, u, items)
+            tile, kb0, kb1, sk_tile, splits, first = items[0]
+            assert splits == pieces and first == (u // pieces) * pieces
+            assert kb1 - kb0 >= 16
+            seen.setdefault(tile, []).append((kb0, kb1))
+        assert sorted(seen) == list(range(T))
+        for tile, ranges in seen.items():
+            ranges.sort()
+            assert ranges[0][0] == 0 and ranges[-1][1] == KB
+            assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
