@@ -192,11 +192,13 @@ class Plan:
 
     def run_host(self, a, b, c, acc="f32", stream=None) -> None:
         """Same on CPU tensors/arrays (pinned for full copy speed); synchronous."""
+        if len(a.shape) != 2 or len(b.shape) != 2 or len(c.shape) != 2:
+            raise ValueError("want A [M,K], B [N,K], C [M,N]")
         M, K = a.shape
         N = b.shape[0]
         if tuple(b.shape) != (N, K) or tuple(c.shape) != (M, N):
             raise ValueError("want A [M,K], B [N,K], C [M,N]")
-        self.run_host_ptr(_host_ptr(a), _host_ptr(b), _host_ptr(c), M, N, K, acc,
+        self.run_host_ptr(_host_ptr(a), _host_ptr(b), _host_ptr(c, writable=True), M, N, K, acc,
                           _stream_handle(stream))
 
     def check_error(self) -> None:
@@ -283,15 +285,24 @@ def _check_tensors(a, b, c):
     return M, N, K, _layout(a, "A"), _layout(b, "B")
 
 
-def _host_ptr(x) -> int:
-    if hasattr(x, "data_ptr"):
-        if x.is_cuda or not x.is_contiguous():
-            raise ValueError("host tensors must be contiguous CPU tensors")
-        return x.data_ptr()
+def _host_ptr(x, writable: bool = False) -> int:
+    """Address of a host buffer the library reads (or, `writable`, writes):
+    a contiguous fp16 CPU tensor or numpy array.  Nothing is converted: a
+    converted copy would be freed when this returns, leaving the library a
+    dangling address, and an output written into a copy would be lost."""
     import numpy as np
-    x = np.asarray(x)
-    if not x.flags.c_contiguous:
-        raise ValueError("host arrays must be C-contiguous")
+    if hasattr(x, "data_ptr"):
+        import torch
+        if x.is_cuda or not x.is_contiguous() or x.dtype != torch.float16:
+            raise ValueError("host tensors must be contiguous float16 CPU tensors")
+        return x.data_ptr()
+    if not isinstance(x, np.ndarray):
+        raise TypeError("host buffers must be numpy arrays or CPU tensors, got %s"
+                        % type(x).__name__)
+    if x.dtype != np.float16 or not x.flags.c_contiguous:
+        raise ValueError("host arrays must be C-contiguous float16")
+    if writable and not x.flags.writeable:
+        raise ValueError("the output array is read-only")
     return x.ctypes.data
 
 

@@ -69,3 +69,31 @@ def test_null_plan_is_rejected_without_touching_cuda(lib):
 
 def test_version(lib):
     assert re.match(r"\d+\.\d+\.\d+", lib.gemm_version().decode())
+
+
+def test_host_buffers_are_taken_as_they_are():
+    """gemm_run_host's binding passes the caller's own buffers: fp16,
+    C-contiguous numpy arrays or CPU tensors.  Anything it would have to
+    convert (a list, another dtype, a strided view) is refused, as is a
+    read-only output, so no address handed to the library can dangle."""
+    import numpy as np
+    import torch
+    a = np.zeros((4, 8), np.float16)
+    assert g._host_ptr(a) == a.ctypes.data
+    t = torch.zeros(4, 8, dtype=torch.float16)
+    assert g._host_ptr(t) == t.data_ptr()
+    with pytest.raises(TypeError):
+        g._host_ptr([[0.0] * 8] * 4)
+    with pytest.raises(ValueError):
+        g._host_ptr(np.zeros((4, 8), np.float32))
+    with pytest.raises(ValueError):
+        g._host_ptr(np.zeros((8, 8), np.float16)[:, ::2])
+    with pytest.raises(ValueError):
+        g._host_ptr(torch.zeros(4, 8))
+    with pytest.raises(ValueError):
+        g._host_ptr(torch.zeros(8, 4, dtype=torch.float16).t())
+    ro = np.zeros((4, 8), np.float16)
+    ro.flags.writeable = False
+    assert g._host_ptr(ro) == ro.ctypes.data
+    with pytest.raises(ValueError):
+        g._host_ptr(ro, writable=True)

@@ -169,6 +169,24 @@ def test_host_entry_point_two_dimensional_blocks(plan):
     assert_close(c[:, cols].astype(np.float64), oracle.gemm_cols_f64(a, b, cols), "f32", "2-D cols")
 
 
+def test_host_entry_point_empty_and_zero_K(plan):
+    """gemm_run_host on the degenerate shapes: K = 0 returns the empty sum
+    (zeros) through the copy-out path; M = 0 or N = 0 touches nothing; a
+    misaligned N is refused before anything is written."""
+    for acc in ("f32", "f16"):
+        out = np.full((40, 24), np.nan, np.float16)
+        plan.run_host(np.zeros((40, 0), np.float16), np.zeros((24, 0), np.float16), out, acc=acc)
+        assert np.array_equal(out.view(np.uint16), np.zeros((40, 24), np.uint16))
+    out = np.full((0, 24), np.nan, np.float16)
+    plan.run_host(np.zeros((0, 16), np.float16), np.ones((24, 16), np.float16), out)
+    keep = np.full((40, 0), np.nan, np.float16)
+    plan.run_host(np.ones((40, 16), np.float16), np.zeros((0, 16), np.float16), keep)
+    bad = np.full((8, 12), np.nan, np.float16)
+    with pytest.raises(g.GemmError):
+        plan.run_host(np.ones((8, 16), np.float16), np.ones((12, 16), np.float16), bad)
+    assert np.isnan(bad).all()
+
+
 def test_gemm_convenience_wrapper(plan):
     a, b = wl.draw(256, 264, 128, seed=35)
     c = g.gemm(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
