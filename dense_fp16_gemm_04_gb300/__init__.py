@@ -183,7 +183,7 @@ class Plan:
         """C = A @ B.T on CUDA tensors: fp16, A [M,K], B [N,K], C [M,N] contiguous.
         A and B may each be contiguous or the transpose of a contiguous tensor
         (A = x.t() with x [K,M]; B = w.t() with w [K,N], i.e. C = A @ w)."""
-        M, N, K, la, lb = _check_tensors(a, b, c)
+        M, N, K, la, lb = _check_tensors(a, b, c, self.device)
         sh = _stream_handle(stream)
         if la == K_CONTIGUOUS and lb == K_CONTIGUOUS:
             self.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, acc, sh)
@@ -266,13 +266,17 @@ def _layout(t, name):
     raise ValueError(f"{name} must be contiguous or the transpose of a contiguous tensor")
 
 
-def _check_tensors(a, b, c):
+def _check_tensors(a, b, c, device=None):
+    """Shapes and layouts of A, B, C; all three must live on the plan's
+    device (the kernel runs there and would fault on another GPU's memory)."""
     import torch
     for name, t in (("A", a), ("B", b), ("C", c)):
         if t.dtype != torch.float16:
             raise TypeError(f"{name} must be float16, got {t.dtype}")
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
+        if device is not None and t.device.index != device:
+            raise ValueError(f"{name} is on cuda:{t.device.index}, the plan on cuda:{device}")
         if t.dim() != 2:
             raise ValueError(f"{name} must be a 2-D tensor")
     if not c.is_contiguous():

@@ -88,8 +88,10 @@ GEMM_API gemm_status_t gemm_plan_create(gemm_plan_t* out, int device);
  * Must not be called while work launched with the plan is still running. */
 GEMM_API gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 
-/* C = A x B^T on device buffers, asynchronously on `stream` (a cudaStream_t;
- * NULL = legacy default stream).
+/* C = A x B^T on device buffers, asynchronously on `stream` (a cudaStream_t
+ * of the plan's device; NULL = legacy default stream).  A, B and C must be
+ * memory of the plan's device: the library does not look the pointers up,
+ * and the kernel would fault on another GPU's memory.
  *   A : device pointer, fp16 [M, K] row-major (K contiguous), 16-byte aligned
  *   B : device pointer, fp16 [N, K] row-major (K contiguous), 16-byte aligned
  *   C : device pointer, fp16 [M, N] row-major, 16-byte aligned, must not
