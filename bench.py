@@ -4,17 +4,25 @@
 One step = one C = A @ B.T over the whole workload (default: M = N = K = 8192,
 fp32 accumulation, fp16 output), inputs resident in HBM.  Prints ONE JSON line
 with TFLOP/s = 2*M*N*K / t, the roofline of the GEMM kernel against the
-measured dense tensor peak, an end-to-end number through the host-buffer
+measured dense tensor peak, the SM clock the kernel itself ran at (its own
+clock record) and the cycles it took per k-block, a seconds-long sustained
+run against the sustained peak, an end-to-end number through the host-buffer
 entry point (host<->device copies inside the timed region), and the CPU
 oracle timed on a bounded sample of the same workload.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--acc f32|f16]
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--acc f32|f16] [--repeat R]
+
+Protocol of the headline number (tilus "Four Consumers, FP16 Accumulation,
+and a TMA Epilogue", section "Performance"): R (default 3) fresh processes,
+each waiting a cool-down (default 3 s) and then timing K back-to-back steps
+with CUDA events; `value` is the median of the R.
 
 --impl reference times the CPU oracle (the plain fp64 triple loop), on the
-host cores, on bounded row samples of the same workload.  For N > 1 (launched
-under torch.distributed.run) every rank runs an independent replica of the
-workload on its own GPU: the GEMM has no exchange step, so scaling is weak.
+host cores, on bounded row samples of the same workload.  The library is for
+one GPU: its ragged-K kernel multicasts TMA loads inside a cluster, which is
+kept out of any multi-GPU run, so under torch.distributed.run with N > 1 rank
+0 prints an "unavailable" line and no rank loads the library.
 """
 from __future__ import annotations
 
@@ -22,6 +30,7 @@ import argparse
 import json
 import os
 import statistics
+import subprocess
 import sys
 import time
 
@@ -36,9 +45,17 @@ import gemm_workloads as wl
 METRIC = "fp16 GEMM TFLOP/s (2MNK/t) and % of GB300 dense fp16 tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_TFLOPS = 1900.0   # used only when the measured-peaks file is absent
+DENSE_FLOP_PER_CLK_SM = 8192   # fp16 tcgen05 rate per SM per clock (measured, see roofline note)
+MULTI_GPU_UNAVAILABLE = (
+    "single-GPU library: its ragged-K kernel (tc_pair_mc_256x256_s6) multicasts TMA loads "
+    "within a cluster, which is kept out of multi-GPU runs; the GEMM has no exchange step")
+
+# Arguments a measuring child process inherits from its parent.
+_CHILD_ARGS = ("steps", "warmup", "workload", "shape", "layout", "acc", "variant", "tile_order",
+               "schedule", "pdl", "cooldown")
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=30)
@@ -47,9 +64,6 @@ def parse():
     p.add_argument("--workload", default="gemm_8192", choices=list(wl.WORKLOADS))
     p.add_argument("--shape", default=None,
                    help="MxNxK: time this shape instead (seeded N(0,1)*K^-1/4 inputs, seed 0)")
-    p.add_argument("--split", default="replicas", choices=["replicas", "m"],
-                   help="N > 1: every rank runs the whole workload (replicas, weak scaling) or "
-                        "its share of C's rows (m, strong scaling)")
     p.add_argument("--layout", default="kk", choices=["kk", "kn", "mk", "mn"],
                    help="storage of A and B: k = K-contiguous, m/n = M/N-contiguous")
     p.add_argument("--acc", default="f32", choices=["f32", "f16"])
@@ -63,11 +77,39 @@ def parse():
     p.add_argument("--graph", action="store_true",
                    help="capture the K timed launches in one CUDA graph (GPU time without "
                         "per-call host overhead; for small shapes)")
+    p.add_argument("--repeat", type=int, default=3,
+                   help="fresh processes timing the K steps; the headline value is their median")
+    p.add_argument("--cooldown", type=float, default=3.0,
+                   help="seconds of idle GPU before each process's timed steps")
+    p.add_argument("--sustained-s", type=float, default=4.0,
+                   help="seconds of back-to-back steps for the sustained leg (0 = skip)")
+    p.add_argument("--child", action="store_true",
+                   help="internal: time the K steps once and print that leg as JSON")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-rows", type=int, default=0,
                    help="oracle sample size in rows (0 = sized for ~10 s)")
-    return p.parse_args()
+    return p.parse_args(argv)
+
+
+def child_argv(args):
+    """Command line of a child process that times the K steps once."""
+    argv = [sys.executable, os.path.abspath(__file__), "--child"]
+    for name in _CHILD_ARGS:
+        v = getattr(args, name)
+        if v is None:
+            continue
+        argv += ["--" + name.replace("_", "-"), str(v)]
+    if args.graph:
+        argv.append("--graph")
+    return argv
+
+
+def median_leg(legs):
+    """The leg whose value is the median of the legs' values (the lower
+    middle one for an even count)."""
+    ranked = sorted(legs, key=lambda d: d["value"])
+    return ranked[(len(ranked) - 1) // 2]
 
 
 def dist_env():
@@ -253,127 +295,240 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
-    import torch
-    import torch.distributed as dist
+class Setup:
+    """The library, a plan with the requested settings, the workload's
+    operands on the GPU and the step function every timed leg runs."""
 
-    import dense_fp16_gemm_04_gb300 as g
+    def __init__(self, args):
+        import torch
 
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+        import dense_fp16_gemm_04_gb300 as g
 
-    g.build()
-    plan = g.Plan(local)
-    if args.variant:
-        plan.set_variant(args.variant)
-    plan.set_tile_order(args.tile_order)
-    plan.set_schedule(args.schedule)
-    plan.set_pdl(args.pdl == "on")
-    w_full = resolve_workload(args)
-    w = w_full
-    a_np, b_np = wl.inputs_for(w_full)
-    if world > 1 and args.split == "m":
-        # This rank's rows of A and C; B whole.  No exchange inside the product.
-        row0, rows = g.shard_rows(w_full.M, world, rank)
-        a_np = np.ascontiguousarray(a_np[row0:row0 + rows])
-        w = wl.Workload(f"{w_full.name}_rows{row0}+{rows}", rows, w_full.N, w_full.K, w_full.seed,
-                        w_full.dist, w_full.accs)
-    la = g.MN_CONTIGUOUS if args.layout[0] == "m" else g.K_CONTIGUOUS
-    lb = g.MN_CONTIGUOUS if args.layout[1] == "n" else g.K_CONTIGUOUS
-    a = torch.from_numpy(a_np if la == g.K_CONTIGUOUS else np.ascontiguousarray(a_np.T)).to(dev)
-    b = torch.from_numpy(b_np if lb == g.K_CONTIGUOUS else np.ascontiguousarray(b_np.T)).to(dev)
-    c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
-    # Operands come from HBM in every step.  When A and B together are larger
-    # than L2 one set streams through it; otherwise the steps rotate over
-    # copies of A, B and C, enough that more than twice L2 is touched between
-    # two uses of the same copy.
-    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    ab_bytes = (a.numel() + b.numel()) * 2
-    set_bytes = ab_bytes + c.numel() * 2
-    n_sets = 1 if ab_bytes > l2_bytes else min(4096, -(-2 * l2_bytes // max(set_bytes, 1)) + 1)
-    sets = [(a, b, c)] + [(a.clone(), b.clone(), torch.empty_like(c)) for _ in range(n_sets - 1)]
-    ptrs = [(x.data_ptr(), y.data_ptr(), z.data_ptr()) for x, y, z in sets]
-    l2_note = ("inputs larger than L2 (A+B = %d MB vs %d MB L2), no flush"
-               % (ab_bytes >> 20, l2_bytes >> 20) if n_sets == 1 else
-               "%d rotating copies of A, B and C (%d MB in all vs %d MB L2): operands from HBM "
-               "every step, no flush" % (n_sets, (n_sets * set_bytes) >> 20, l2_bytes >> 20))
+        self.torch, self.g = torch, g
+        torch.cuda.set_device(0)
+        self.dev = dev = torch.device("cuda", 0)
+        g.build()
+        self.plan = plan = g.Plan(0)
+        if args.variant:
+            plan.set_variant(args.variant)
+        plan.set_tile_order(args.tile_order)
+        plan.set_schedule(args.schedule)
+        plan.set_pdl(args.pdl == "on")
+        self.w = w = resolve_workload(args)
+        self.acc = args.acc
+        self.a_np, self.b_np = wl.inputs_for(w)
+        la = g.MN_CONTIGUOUS if args.layout[0] == "m" else g.K_CONTIGUOUS
+        lb = g.MN_CONTIGUOUS if args.layout[1] == "n" else g.K_CONTIGUOUS
+        self.kk = la == g.K_CONTIGUOUS and lb == g.K_CONTIGUOUS
+        self.la, self.lb = la, lb
+        a = torch.from_numpy(self.a_np if la == g.K_CONTIGUOUS
+                             else np.ascontiguousarray(self.a_np.T)).to(dev)
+        b = torch.from_numpy(self.b_np if lb == g.K_CONTIGUOUS
+                             else np.ascontiguousarray(self.b_np.T)).to(dev)
+        c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        # Operands come from HBM in every step.  When A and B together are
+        # larger than L2 one set streams through it; otherwise the steps
+        # rotate over copies of A, B and C, enough that more than twice L2 is
+        # touched between two uses of the same copy.
+        l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+        ab_bytes = (a.numel() + b.numel()) * 2
+        set_bytes = ab_bytes + c.numel() * 2
+        self.n_sets = n_sets = (1 if ab_bytes > l2_bytes else
+                                min(4096, -(-2 * l2_bytes // max(set_bytes, 1)) + 1))
+        sets = [(a, b, c)] + [(a.clone(), b.clone(), torch.empty_like(c))
+                              for _ in range(n_sets - 1)]
+        self.sets = sets
+        self.ptrs = [(x.data_ptr(), y.data_ptr(), z.data_ptr()) for x, y, z in sets]
+        self.l2_note = (
+            "inputs larger than L2 (A+B = %d MB vs %d MB L2), no flush"
+            % (ab_bytes >> 20, l2_bytes >> 20) if n_sets == 1 else
+            "%d rotating copies of A, B and C (%d MB in all vs %d MB L2): operands from HBM "
+            "every step, no flush" % (n_sets, (n_sets * set_bytes) >> 20, l2_bytes >> 20))
 
-    def step(i, stream_handle=sh):
-        aptr, bptr, cptr = ptrs[i % n_sets]
-        if la == g.K_CONTIGUOUS and lb == g.K_CONTIGUOUS:
-            plan.run_ptr(aptr, bptr, cptr, w.M, w.N, w.K, args.acc, stream_handle)
+    def step(self, i, stream_handle=None):
+        sh = self.stream.cuda_stream if stream_handle is None else stream_handle
+        aptr, bptr, cptr = self.ptrs[i % self.n_sets]
+        w = self.w
+        if self.kk:
+            self.plan.run_ptr(aptr, bptr, cptr, w.M, w.N, w.K, self.acc, sh)
         else:
-            plan.run_ex_ptr(aptr, la, bptr, lb, cptr, w.M, w.N, w.K, args.acc, stream_handle)
+            self.plan.run_ex_ptr(aptr, self.la, bptr, self.lb, cptr, w.M, w.N, w.K, self.acc, sh)
 
+    def sync(self):
+        self.torch.cuda.synchronize(self.dev)
+
+    def kblocks_per_unit(self):
+        """k-blocks (64 deep) each persistent unit runs per launch, and the
+        cycles one k-block of that unit's tile needs at the dense rate."""
+        w = self.w
+        d = self.plan.describe(w.M, w.N, w.K, self.acc)
+        num_kb = -(-w.K // 64)
+        total = d["dp_tiles"] * num_kb + d["sk_iters"]
+        units = max(1, d["units"])
+        vi = self.g.variant_info(d["variant"])
+        ideal = vi["tile_m"] * vi["tile_n"] * 64 * 2 / (DENSE_FLOP_PER_CLK_SM * vi["ctas"])
+        return total / units, ideal, d
+
+
+def device_leg(args, su):
+    """Warm up, wait the cool-down, then time K back-to-back steps with one
+    CUDA event pair on the launching stream; NVML clocks are sampled during
+    the steps and the kernels' own clock record is read after them."""
+    torch, plan = su.torch, su.plan
     n_warm = max(args.warmup, 3)
     for i in range(n_warm):
-        step(i)
+        su.step(i)
     plan.check_error()
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-
-    # ----------------------------------------------------- device-timed run --
-    # One event pair around the K steps: no event sits between two launches,
-    # so each GEMM's set-up may overlap the end of the previous one
-    # (programmatic dependent launch, as in any back-to-back use).
-    launches0 = plan.launch_count
     graph = None
     if args.graph:
-        cap = torch.cuda.Stream(dev)
+        cap = torch.cuda.Stream(su.dev)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap):
             for i in range(args.steps):
-                step(n_warm + i, cap.cuda_stream)
+                su.step(n_warm + i, cap.cuda_stream)
         graph.replay()
-        torch.cuda.synchronize(dev)
-        launches0 = plan.launch_count
-    sampler = ClockSampler(dev)
-    barrier()
+        su.sync()
+    if args.cooldown > 0:
+        time.sleep(args.cooldown)
+    plan.kernel_clock()                      # start the clock record from zero
+    launches0 = plan.launch_count
+    sampler = ClockSampler(su.dev)
+    su.sync()
     with sampler:
-        t_all0 = torch.cuda.Event(enable_timing=True)
-        t_all1 = torch.cuda.Event(enable_timing=True)
-        t_all0.record(stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(su.stream)
         if graph is not None:
             graph.replay()
         else:
             for i in range(args.steps):
-                step(n_warm + i)
-        t_all1.record(stream)
-        barrier()
+                su.step(n_warm + i)
+        e1.record(su.stream)
+        su.sync()
     launches = plan.launch_count - launches0 if graph is None else args.steps
     plan.check_error()
-    total_ms = reduce_max(t_all0.elapsed_time(t_all1), world, dev)
-    per_launch_ms = [t_all0.elapsed_time(t_all1) / args.steps]
-    clocks = sampler.summary()
+    kclk = plan.kernel_clock()
+    ms = e0.elapsed_time(e1) / args.steps
+    w = su.w
+    kb_unit, ideal, d = su.kblocks_per_unit()
+    cyc = ms * 1e-3 * kclk["mhz"] * 1e6 if kclk["mhz"] else None
+    return {"leg": "device", "value": w.flops / (ms * 1e-3) / 1e12, "ms_per_step": ms,
+            "steps": args.steps, "gpu_launches": int(launches), "clocks": sampler.summary(),
+            "kernel_clock": {"mhz": kclk["mhz"], "launches": kclk["launches"],
+                             "source": "the kernel's own record: %clock64 over %globaltimer "
+                                       "across CTA 0's lifetime, summed over the timed launches"},
+            "cycles_per_kblock": cyc / kb_unit if cyc else None,
+            "ideal_cycles_per_kblock": ideal, "kblocks_per_unit": kb_unit,
+            "units": d["units"], "variant": d["variant"], "grid_ctas": d["grid_ctas"]}
 
-    flops = float(w.flops)
-    strong = world > 1 and args.split == "m"
-    # replicas: every rank did its own full problem; m: the ranks together did one.
-    value = (aggregate_tflops(1, args.steps, float(w_full.flops), total_ms * 1e-3) if strong
-             else aggregate_tflops(world, args.steps, flops, total_ms * 1e-3))
-    ms_per_step = total_ms / args.steps
+
+def sustained_leg(args, su, seconds, step_ms):
+    """Back-to-back steps for about `seconds` between one CUDA event pair,
+    long enough for the board's power limit to set the SM clock."""
+    torch, plan = su.torch, su.plan
+    n = max(args.steps, int(seconds * 1e3 / max(step_ms, 1e-3)) + 1)
+    for i in range(3):
+        su.step(i)
+    su.sync()
+    plan.kernel_clock()
+    sampler = ClockSampler(su.dev, period_s=0.02)
+    with sampler:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(su.stream)
+        for i in range(n):
+            su.step(i)
+        e1.record(su.stream)
+        su.sync()
+    plan.check_error()
+    kclk = plan.kernel_clock()
+    total_ms = e0.elapsed_time(e1)
+    return {"value": n * su.w.flops / (total_ms * 1e-3) / 1e12, "unit": UNIT,
+            "seconds": total_ms * 1e-3, "steps": n, "ms_per_step": total_ms / n,
+            "clocks": sampler.summary(), "kernel_mhz": kclk["mhz"]}
+
+
+def e2e_leg(args, su):
+    """The same product through gemm_run_host: pinned host buffers, the
+    host->device copies of A and B and the device->host copy of C inside
+    every timed step (the call is synchronous)."""
+    torch, plan, w = su.torch, su.plan, su.w
+    ha = torch.from_numpy(su.a_np).pin_memory()
+    hb = torch.from_numpy(su.b_np).pin_memory()
+    hc = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+    hp = (ha.data_ptr(), hb.data_ptr(), hc.data_ptr())
+    sh = su.stream.cuda_stream
+    for _ in range(2):
+        plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)
+    e_steps = max(3, min(args.steps, 10))
+    su.sync()
+    t0 = time.perf_counter()
+    marks = []
+    for _ in range(e_steps):
+        plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)  # synchronous
+        marks.append(time.perf_counter())
+    dt = marks[-1] - t0
+    step_ms = sorted((b - a) * 1e3 for a, b in zip([t0] + marks[:-1], marks))
+    return {"value": e_steps * w.flops / dt / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": int(su.a_np.nbytes + su.b_np.nbytes),
+            "d2h_bytes_per_step": int(w.M * w.N * 2),
+            "ms_per_step": dt / e_steps * 1e3, "steps": e_steps,
+            # the steps one by one: a host-link hiccup shows here
+            "step_ms": {"min": step_ms[0], "median": step_ms[len(step_ms) // 2],
+                        "max": step_ms[-1]}}
+
+
+def run_child(args):
+    su = Setup(args)
+    leg = device_leg(args, su)
+    su.plan.close()
+    print(json.dumps(leg), flush=True)
+    return 0
+
+
+def run_ours(args):
+    rank, world, _ = dist_env()
+    if world > 1:
+        # One GPU only (see the module docstring): nothing is loaded.
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "unit": UNIT, "n_gpus": world,
+                              "higher_is_better": True, "unavailable": MULTI_GPU_UNAVAILABLE}),
+                  flush=True)
+        return 0
+    if args.child:
+        return run_child(args)
+
+    # ---------------------------------------- headline: R fresh processes --
+    legs = []
+    if args.repeat > 1:
+        for _ in range(args.repeat):
+            r = subprocess.run(child_argv(args), capture_output=True, text=True)
+            if r.returncode != 0:
+                sys.stderr.write(r.stdout + r.stderr)
+                raise SystemExit(f"measuring process failed (rc {r.returncode})")
+            legs.append(json.loads([ln for ln in r.stdout.splitlines() if ln.strip()][-1]))
+    su = Setup(args)
+    if args.repeat <= 1:
+        legs.append(device_leg(args, su))
+    head = median_leg(legs)
+    w = su.w
+
     peaks = measured_peaks()
+    clocks = head["clocks"]
     # The burst peak for a kernel timed alone; once the power cap has acted
     # inside the timed region (a long step), the sustained one.
-    sustained = "sw_power_cap" in (clocks.get("reasons") or [])
-    peak = peaks["tflops_sustained"] if sustained else peaks["tflops"]
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    peak = peaks["tflops_sustained"] if capped else peaks["tflops"]
     peak_source = "%s bf16 %s (fp16 1:1)" % (peaks["source"],
-                                            "sustained: power cap active" if sustained else "burst")
-    kernel_ms = statistics.mean(per_launch_ms)
-    achieved = flops / (kernel_ms * 1e-3) / 1e12
+                                            "sustained: power cap active" if capped else "burst")
+    kernel_ms = head["ms_per_step"]
+    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
     # Roofline of the kernel: algorithmic bytes 2(MK + NK + MN) against the
     # measured copy bandwidth when the arithmetic intensity is below the
     # ridge (C with few rows: HBM-bound), else FLOP against the tensor peak.
     alg_bytes = 2.0 * (w.M * w.K + w.N * w.K + w.M * w.N)
-    hbm_bound = flops / alg_bytes < peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    hbm_bound = w.flops / alg_bytes < peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": alg_bytes / (kernel_ms * 1e-3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -383,66 +538,52 @@ def run_ours(args):
                 "peak_source": peak_source}
     roof["frac"] = roof["achieved"] / roof["peak"]
 
-    # ------------------------------------------------- end to end, host API --
-    e2e = None
-    if not args.no_e2e and args.layout == "kk":
-        ha = torch.from_numpy(a_np).pin_memory()
-        hb = torch.from_numpy(b_np).pin_memory()
-        hc = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
-        hp = (ha.data_ptr(), hb.data_ptr(), hc.data_ptr())
-        for _ in range(2):
-            plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)
-        e_steps = max(3, min(args.steps, 10))
-        barrier()
-        t0 = time.perf_counter()
-        marks = []
-        for _ in range(e_steps):
-            plan.run_host_ptr(*hp, w.M, w.N, w.K, args.acc, sh)  # synchronous
-            marks.append(time.perf_counter())
-        dt = reduce_max(marks[-1] - t0, world, dev)
-        step_ms = sorted((b - a) * 1e3 for a, b in zip([t0] + marks[:-1], marks))
-        e2e = {"value": (aggregate_tflops(1, e_steps, float(w_full.flops), dt) if strong
-                         else aggregate_tflops(world, e_steps, flops, dt)), "unit": UNIT,
-               "h2d_bytes_per_step": int(a_np.nbytes + b_np.nbytes),
-               "d2h_bytes_per_step": int(w.M * w.N * 2),
-               "ms_per_step": dt / e_steps * 1e3, "steps": e_steps,
-               # this rank's steps one by one: a host-link hiccup shows here
-               "step_ms": {"min": step_ms[0], "median": step_ms[len(step_ms) // 2],
-                           "max": step_ms[-1]}}
+    # ------------------------------------------------ sustained, end to end --
+    sustained = None
+    if args.sustained_s > 0:
+        sustained = sustained_leg(args, su, args.sustained_s, kernel_ms)
+        sustained["peak"] = peaks["tflops_sustained"]
+        sustained["peak_source"] = peaks["source"] + " bf16 sustained (fp16 1:1)"
+        sustained["frac"] = sustained["value"] / sustained["peak"]
+    e2e = e2e_leg(args, su) if not args.no_e2e and args.layout == "kk" else None
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, used, sample, _ = cpu_oracle_rate(w, args.cpu_rows, steps=1, a=a_np, b=b_np)
+    if not args.no_cpu_baseline:
+        rate, used, sample, _ = cpu_oracle_rate(w, args.cpu_rows, steps=1, a=su.a_np, b=su.b_np)
         cpu = {"value": rate, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample}
 
     # The recorded ncu traffic is for the automatic settings only.
     defaults = (args.layout == "kk" and args.schedule == "auto" and args.tile_order == "auto"
-                and args.pdl == "on")
-    traffic = (_recorded_traffic(w.name, args.acc, plan.pick_variant(w.M, w.N, w.K, args.acc)[0])
-               if defaults else None)
-    variant, grid = plan.pick_variant(w.M, w.N, w.K, args.acc)
+                and args.pdl == "on" and not args.variant)
+    traffic = _recorded_traffic(w.name, args.acc, head["variant"]) if defaults else None
+    kclk = dict(head["kernel_clock"])
+    kclk["cycles_per_kblock"] = head["cycles_per_kblock"]
+    kclk["ideal_cycles_per_kblock"] = head["ideal_cycles_per_kblock"]
+    kclk["kblocks_per_unit"] = head["kblocks_per_unit"]
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "strong" if strong else "weak", "vs_baseline": None,
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": kernel_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic",
-        "config": {"workload": f"{w_full.name}: {w_full.describe()}", "M": w_full.M, "N": w.N, "K": w.K,
-                   "acc": args.acc, "layout": args.layout, "variant": variant, "grid_ctas": grid,
-                   "l2": l2_note,
-                   "parallelism": (f"M split x{world}" if strong else f"replicas x{world}")
-                                  if world > 1 else "single GPU",
-                   "launch": "CUDA graph of the K steps" if graph is not None else "one call per step",
+        "config": {"workload": f"{w.name}: {w.describe()}", "M": w.M, "N": w.N, "K": w.K,
+                   "acc": args.acc, "layout": args.layout, "variant": head["variant"],
+                   "grid_ctas": head["grid_ctas"], "l2": su.l2_note, "parallelism": "single GPU",
+                   "launch": "CUDA graph of the K steps" if args.graph else "one call per step",
                    "schedule": args.schedule, "tile_order": args.tile_order, "pdl": args.pdl},
-        "pct_of_peak": value / world / peak,
+        "repeats": {"n": len(legs), "values": [d["value"] for d in legs],
+                    "kernel_mhz": [d["kernel_clock"]["mhz"] for d in legs],
+                    "how": ("median of %d fresh processes, each after a %.0f s cool-down"
+                            % (len(legs), args.cooldown)) if len(legs) > 1 else
+                           "one process, after a %.0f s cool-down" % args.cooldown},
+        "pct_of_peak": head["value"] / peak,
         "roofline": {**roof, "traffic": traffic},
-        "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
+        "clocks": clocks, "kernel_clock": kclk,
+        "cycles_per_kblock": head["cycles_per_kblock"],
+        "sustained": sustained, "e2e": e2e, "gpu_launches": head["gpu_launches"],
         "cpu_baseline": cpu,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    plan.close()
-    if world > 1:
-        dist.destroy_process_group()
+    print(json.dumps(line), flush=True)
+    su.plan.close()
     return 0
 
 
@@ -478,23 +619,6 @@ def _recorded_traffic(workload, acc, variant):
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
     return int(e["dram_bytes_per_launch"])
-
-
-def reduce_max(x: float, world: int, device=None) -> float:
-    """Max of a per-rank scalar over all ranks (identity for one rank)."""
-    if world <= 1:
-        return float(x)
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def aggregate_tflops(world: int, steps: int, flops_per_step: float, seconds: float) -> float:
-    """Whole-job throughput: every rank runs `steps` steps of `flops_per_step`
-    in `seconds` (the slowest rank's time)."""
-    return world * steps * flops_per_step / seconds / 1e12
 
 
 def main():

@@ -24,8 +24,8 @@ import threading
 from . import _build
 
 __all__ = [
-    "build", "load", "Plan", "GemmError", "gemm", "gemm_host", "default_plan", "shard_rows",
-    "ACC_F32", "ACC_F16", "K_CONTIGUOUS", "MN_CONTIGUOUS", "status_string", "variant_names",
+    "build", "load", "Plan", "GemmError", "gemm", "gemm_host", "default_plan",
+    "ACC_F32", "ACC_F16", "K_CONTIGUOUS", "MN_CONTIGUOUS", "status_string", "variant_names", "variant_info",
     "LIB_PATH",
 ]
 
@@ -90,9 +90,12 @@ def load():
                                          ctypes.POINTER(ctypes.c_int64)]),
             "gemm_variant_count": (i32, []),
             "gemm_variant_name": (ctypes.c_char_p, [i32]),
+            "gemm_variant_info": (i32, [i32, ctypes.POINTER(i32)]),
+            "gemm_plan_resident_units": (st, [vp, ctypes.POINTER(i32)]),
             "gemm_plan_pick_variant": (i32, [vp, i64, i64, i64, ctypes.c_int,
                                              ctypes.POINTER(i32)]),
             "gemm_plan_launch_count": (u64, [vp]),
+            "gemm_plan_kernel_clock": (st, [vp, ctypes.POINTER(u64)]),
             "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "gemm_version": (ctypes.c_char_p, []),
         }
@@ -111,6 +114,17 @@ def status_string(status: int) -> str:
 def variant_names():
     lib = load()
     return [lib.gemm_variant_name(i).decode() for i in range(lib.gemm_variant_count())]
+
+
+def variant_info(variant) -> dict:
+    """CTAs per unit, the unit's tile of C (rows x columns) and whether the
+    MMA roles are swapped, for a variant given by name or index."""
+    if isinstance(variant, str):
+        variant = variant_names().index(variant)
+    out = (ctypes.c_int32 * 4)()
+    if load().gemm_variant_info(int(variant), out) != 0:
+        raise ValueError(f"unknown variant {variant!r}")
+    return {"ctas": out[0], "tile_m": out[1], "tile_n": out[2], "swap": bool(out[3])}
 
 
 def _check(status: int, where: str):
@@ -251,6 +265,22 @@ class Plan:
             raise GemmError(1, "gemm_plan_pick_variant")
         return variant_names()[v], grid.value
 
+    def resident_units(self) -> dict:
+        """Units of each kind that fit on the device at once."""
+        out = (ctypes.c_int32 * 3)()
+        _check(self._lib.gemm_plan_resident_units(self._h, out), "gemm_plan_resident_units")
+        return {"ctas": out[0], "pairs": out[1], "quads": out[2]}
+
+    def kernel_clock(self) -> dict:
+        """Synchronize, then read and reset the kernels' own clock record:
+        launches since the last read, CTA 0's lifetime summed in SM cycles and
+        in ns, and their ratio, the mean SM clock (MHz) the kernels ran at."""
+        out = (ctypes.c_uint64 * 3)()
+        _check(self._lib.gemm_plan_kernel_clock(self._h, out), "gemm_plan_kernel_clock")
+        launches, cycles, ns = int(out[0]), int(out[1]), int(out[2])
+        return {"launches": launches, "cycles": cycles, "ns": ns,
+                "mhz": cycles * 1e3 / ns if ns else None}
+
     @property
     def launch_count(self) -> int:
         return int(self._lib.gemm_plan_launch_count(self._h))
@@ -347,19 +377,3 @@ def gemm_host(a, b, acc="f32", out=None, stream=None, plan: Plan | None = None):
                           pin_memory=bool(getattr(a, "is_pinned", lambda: False)()))
     (plan or default_plan()).run_host(a, b, out, acc=acc, stream=stream)
     return out
-
-
-def shard_rows(M: int, world: int, rank: int, align: int = 256):
-    """Rows [row0, row0 + rows) of C (and A) owned by `rank` of `world` when one
-    GEMM is split over GPUs by rows: each rank multiplies its rows of A by all
-    of B, with no exchange inside the product.  Shard starts are multiples of
-    `align` (a whole number of 256-row tiles) except where M itself ends, and
-    the shards cover [0, M) exactly once."""
-    if world < 1 or not 0 <= rank < world:
-        raise ValueError("need 0 <= rank < world")
-    tiles = -(-M // align)
-    t0 = tiles * rank // world
-    t1 = tiles * (rank + 1) // world
-    row0 = min(M, t0 * align)
-    row1 = min(M, t1 * align)
-    return row0, row1 - row0

@@ -79,6 +79,7 @@ constexpr VariantInfo kVariants[kNumVariants] = {
 };
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s for any single wait
+constexpr size_t kRecordBytes = 64;  // watchdog record (16 B) + clock record (3 x 8 B)
 constexpr int kGroupM = 8;                             // raster group height, tiles
 constexpr int kMapCacheSize = 32;
 // gemm_run_host's pipeline: at most kHostChunksA row chunks of A and
@@ -114,7 +115,8 @@ struct gemm_plan_s {
   int32_t tile_order = 0;  // 0 automatic, 1 static round robin, 2 dynamic when possible
   int32_t schedule_mode = 0;  // 0 auto, 1 whole tiles only, 2 stream-K tail whenever possible
   EncodeTiledFn encode = nullptr;
-  uint32_t* d_err = nullptr;  // 4-word watchdog record
+  uint32_t* d_err = nullptr;  // 4-word watchdog record, then the clock record
+  unsigned long long* d_clk = nullptr;  // [launches, SM cycles, ns] of CTA 0 (inside d_err's block)
   uint32_t last_err[4] = {0, 0, 0, 0};
   uint64_t timeout_ns = kDefaultTimeoutNs;
   int32_t skip_kb = -1;
@@ -152,9 +154,36 @@ struct DeviceGuard {
   }
 };
 
-// Row-major fp16 [rows, cols] whose rows are `pitch` elements apart (0: cols).
-bool get_map(gemm_plan_s* p, CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols,
-             uint32_t box_rows, uint32_t box_cols, uint64_t pitch = 0) {
+// L2 promotion of the operand loads.  Rows whose pitch is not a multiple of
+// 128 bytes straddle L2 lines; there promoting each request to 256 bytes
+// costs more than it saves (measured ~6% slower at K = 4104), so promote by
+// 128 bytes.
+CUtensorMapL2promotion l2_promotion(uint64_t pitch_bytes) {
+  return pitch_bytes % 128 == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+}
+
+// True if `ptr` lies in memory allocated on device `dev` (cudaMalloc,
+// cudaMallocAsync, or virtual memory mapped there).  Host, managed and
+// unregistered memory, and another GPU's memory, are refused: the kernel's
+// tensor maps must cover this GPU's own memory.
+bool on_device(const void* ptr, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+enum MapResult { kMapOk = 0, kMapNotDevice = 1, kMapEncodeFailed = 2 };
+
+// Tensor map of a row-major fp16 [rows, cols] whose rows are `pitch`
+// elements apart (0: cols), from the plan's cache.  A pointer is checked to be
+// memory of the plan's device when its map is made (a cache miss): a cached
+// map stands for a pointer already checked.
+MapResult get_map(gemm_plan_s* p, CUtensorMap* out, const void* ptr, uint64_t rows,
+                  uint64_t cols, uint32_t box_rows, uint32_t box_cols, uint64_t pitch = 0) {
   if (pitch == 0) pitch = cols;
   MapEntry* victim = &p->maps[0];
   for (int i = 0; i < kMapCacheSize; ++i) {
@@ -163,26 +192,23 @@ bool get_map(gemm_plan_s* p, CUtensorMap* out, const void* ptr, uint64_t rows, u
         e.box_rows == box_rows && e.box_cols == box_cols) {
       e.stamp = ++p->clock;
       *out = e.map;
-      return true;
+      return kMapOk;
     }
     if (e.stamp < victim->stamp) victim = &e;
   }
+  if (!on_device(ptr, p->device)) return kMapNotDevice;
   // Row-major fp16 [rows, cols]: dimension 0 is the contiguous one.
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {pitch * 2};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  // Rows whose pitch is not a multiple of 128 bytes straddle L2 lines; then
-  // promoting each request to 256 bytes costs more than it saves (measured
-  // ~6% slower at K = 4104), so promote by 128 bytes there.
-  const CUtensorMapL2promotion promo = (pitch * 2) % 128 == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-                                                             : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
   CUresult r = p->encode(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr),
                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(pitch * 2),
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     victim->stamp = 0;
-    return false;
+    return kMapEncodeFailed;
   }
   victim->ptr = ptr;
   victim->rows = rows;
@@ -192,7 +218,7 @@ bool get_map(gemm_plan_s* p, CUtensorMap* out, const void* ptr, uint64_t rows, u
   victim->box_cols = box_cols;
   victim->stamp = ++p->clock;
   *out = victim->map;
-  return true;
+  return kMapOk;
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -272,7 +298,9 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
   const VariantInfo& vi = kVariants[v];
   const int64_t T = tiles_of(vi, M, N);
   const int64_t KB = (K + 63) / 64;
-  const int64_t U = vi.ctas == 4 ? p->max_quads : vi.ctas == 2 ? p->max_pairs : p->num_sms;
+  const int64_t U = vi.ctas == 4   ? p->max_quads
+                    : vi.ctas == 2 ? p->max_pairs
+                                   : p->num_sms;
   Schedule s;
   s.variant = v;
   s.units = T < U ? T : U;
@@ -405,7 +433,7 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
                          int la = GEMM_K_CONTIGUOUS, int lb = GEMM_K_CONTIGUOUS, int64_t ldc = 0) {
   if (ldc == 0) ldc = N;
   if (K == 0) {
-    if (ldc != N) return GEMM_ERR_INVALID_ARG;
+    if (ldc != N || !on_device(C, p->device)) return GEMM_ERR_INVALID_ARG;
     const int64_t n16 = M * N * 2 / 16;
     const int64_t blocks = (n16 + 255) / 256;
     gb300::gemm_zero_fill<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0,
@@ -424,11 +452,12 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   // K-contiguous operands: boxes of 64 K-elements x the tile's rows.
   // M/N-contiguous operands (stored [K, M] / [K, N]): boxes of 64 x 64.
   CUtensorMap ma, mb, mc;
-  const bool maps_ok =
-      (a_mn ? get_map(p, &ma, A, K, M, 64, 64) : get_map(p, &ma, A, M, K, vi.box_a_rows, 64)) &&
-      (b_mn ? get_map(p, &mb, B, K, N, 64, 64) : get_map(p, &mb, B, N, K, vi.box_b_rows, 64)) &&
-      get_map(p, &mc, C, M, N, 32, 64, static_cast<uint64_t>(ldc));
-  if (!maps_ok) return GEMM_ERR_CUDA;
+  MapResult mr =
+      a_mn ? get_map(p, &ma, A, K, M, 64, 64) : get_map(p, &ma, A, M, K, vi.box_a_rows, 64);
+  if (mr == kMapOk)
+    mr = b_mn ? get_map(p, &mb, B, K, N, 64, 64) : get_map(p, &mb, B, N, K, vi.box_b_rows, 64);
+  if (mr == kMapOk) mr = get_map(p, &mc, C, M, N, 32, 64, static_cast<uint64_t>(ldc));
+  if (mr != kMapOk) return mr == kMapNotDevice ? GEMM_ERR_INVALID_ARG : GEMM_ERR_CUDA;
 
   GemmArgs args;
   args.M = static_cast<int32_t>(M);
@@ -459,6 +488,7 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   args.sk_ws = p->sk_ws;
   args.sk_count = p->sk_count;
   args.tile_ctr = sch.dyn ? p->tile_ctr : nullptr;
+  args.clk = p->d_clk;
 
   const bool f32 = acc == GEMM_ACC_F32;
   cudaError_t e;
@@ -539,6 +569,23 @@ const char* gemm_status_string(gemm_status_t s) {
 
 int32_t gemm_variant_count(void) { return kNumVariants; }
 
+int32_t gemm_variant_info(int32_t v, int32_t out[4]) {
+  if (v < 0 || v >= kNumVariants || !out) return -1;
+  out[0] = kVariants[v].ctas;
+  out[1] = kVariants[v].tile_m;
+  out[2] = kVariants[v].tile_n;
+  out[3] = kVariants[v].swap ? 1 : 0;
+  return 0;
+}
+
+gemm_status_t gemm_plan_resident_units(gemm_plan_t p, int32_t out[3]) {
+  if (!p || !out) return GEMM_ERR_INVALID_ARG;
+  out[0] = p->num_sms;
+  out[1] = p->max_pairs;
+  out[2] = p->max_quads;
+  return GEMM_OK;
+}
+
 const char* gemm_variant_name(int32_t v) {
   return (v >= 0 && v < kNumVariants) ? kVariants[v].name : nullptr;
 }
@@ -592,11 +639,13 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     const int q0 = max_active_clusters<PairMcF32>(), q1 = max_active_clusters<PairMcF16>();
     p->max_quads = q0 < q1 ? q0 : q1;
   }
-  if (cudaMalloc(&p->d_err, 4 * sizeof(uint32_t)) != cudaSuccess) {
+  // 16-byte watchdog record, then three 8-byte clock counters.
+  if (cudaMalloc(&p->d_err, kRecordBytes) != cudaSuccess) {
     delete p;
     return GEMM_ERR_OOM;
   }
-  if (cudaMemset(p->d_err, 0, 4 * sizeof(uint32_t)) != cudaSuccess) {
+  p->d_clk = reinterpret_cast<unsigned long long*>(p->d_err + 4);
+  if (cudaMemset(p->d_err, 0, kRecordBytes) != cudaSuccess) {
     cudaFree(p->d_err);
     delete p;
     return GEMM_ERR_CUDA;
@@ -767,6 +816,19 @@ gemm_status_t gemm_plan_check_error(gemm_plan_t p) {
 gemm_status_t gemm_plan_last_error_detail(gemm_plan_t p, uint32_t detail[4]) {
   if (!p || !detail) return GEMM_ERR_INVALID_ARG;
   std::memcpy(detail, p->last_err, sizeof(p->last_err));
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_kernel_clock(gemm_plan_t p, uint64_t out[3]) {
+  if (!p || !out) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  unsigned long long rec[3] = {0, 0, 0};
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(rec, p->d_clk, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(p->d_clk, 0, sizeof(rec)) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  for (int i = 0; i < 3; ++i) out[i] = static_cast<uint64_t>(rec[i]);
   return GEMM_OK;
 }
 
@@ -958,7 +1020,7 @@ bool noalloc_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
   cuuint32_t estr[2] = {1, 1};
   return g_noalloc_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(cols * 2),
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -981,6 +1043,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return GEMM_ERR_CUDA;
   if (dev >= kNoAllocMaxDevices) return GEMM_ERR_INVALID_ARG;
+  if (!on_device(C, dev) || (K > 0 && (!on_device(A, dev) || !on_device(B, dev))))
+    return GEMM_ERR_INVALID_ARG;
   NoAllocDevice& d = g_noalloc_dev[dev];
   std::call_once(d.once, [&] { d.status = noalloc_setup(dev, d); });
   if (d.status != GEMM_OK) return d.status;
@@ -1019,6 +1083,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   args.sk_ws = nullptr;
   args.sk_count = nullptr;
   args.tile_ctr = nullptr;  // static tile order: no counters here
+  args.clk = nullptr;       // no clock record either
   args.C = static_cast<uint16_t*>(C);
   args.ldc = N;
   args.a_mn = 0;

@@ -104,6 +104,10 @@ struct GemmArgs {
   // Dynamic order of whole tiles: [0] tickets taken, [1] units finished (both
   // back to zero when a launch ends).  nullptr: the static round robin.
   uint32_t* tile_ctr;
+  // Clock record, or nullptr: CTA 0 adds 1, its lifetime in SM cycles
+  // (%clock64) and in ns (%globaltimer) to [0], [1], [2], so the host can
+  // read the SM clock the kernel actually ran at.
+  unsigned long long* clk;
 };
 
 struct Watch {
@@ -291,14 +295,15 @@ struct GemmCfg {
   // loading half of its 128 rows and multicasting it to the CTA in the same
   // position of the other pair, so every SM requests half as many A bytes.
   static constexpr int kMc = kMc_;
-  static constexpr int kClusterCtas = kCtas * kMc;
+  static constexpr int kPairs = kMc;  // CTA pairs (or lone CTAs) per cluster
+  static constexpr int kClusterCtas = kCtas * kPairs;
   // Swapped roles (for small M): the MMA's "A" operand is a 128-row tile of B
   // and its "B" operand a kBN-row tile of A, so D = tile of C^T.
   static constexpr bool kSwap = kSwap_;
   static constexpr int kBM = 128;                 // rows of C per CTA
   static constexpr int kBN = kBN_;                // columns of C per tile
   static constexpr int kBK = 64;                  // K per stage (one 128-byte swizzle row)
-  static constexpr int kTileM = kBM * kCtas;      // rows of C per tile
+  static constexpr int kTileM = kBM * kCtas;      // rows of C per tile (of one pair)
   static constexpr int kBRows = kBN / kCtas;      // rows of B each CTA loads
   static constexpr int kStages = kStages_;
   static constexpr bool kAccF16 = kAccF16_;
@@ -328,12 +333,13 @@ struct GemmCfg {
   static constexpr int kThreads = 256;
   // Warps that read the tile ring: in every CTA both producers and the four
   // epilogue warps, and the MMA issuer in each pair's (or lone CTA's) leader.
-  static constexpr int kTileConsumers = kClusterCtas * (2 + kEpiWarps) + (kCtas == 1 ? 1 : kMc);
+  static constexpr int kTileConsumers = kClusterCtas * (2 + kEpiWarps) + (kCtas == 1 ? 1 : kPairs);
   static constexpr uint32_t kIdesc = ptx::idesc_f16(kTileM, kBN, !kAccF16);
 
   static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair");
   static_assert(kMc == 1 || (kMc == 2 && kCtas == 2 && !kSwap),
                 "A multicast between two CTA pairs only");
+  static_assert(kClusterCtas <= 8, "portable cluster size");
   static_assert(kSwap ? (kCtas == 1 && (kBN == 16 || kBN == 32 || kBN == 64))
                       : (kBN == 64 || kBN == 128 || kBN == 256),
                 "tile width: 64, 128 or 256; 16, 32 or 64 with swapped roles (one CTA)");
@@ -373,6 +379,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   constexpr int S = Cfg::kStages;
   constexpr bool kPair = Cfg::kCtas == 2;
+  // CTA 0's start, for the clock record.
+  const bool clk_cta = args.clk != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
+  const uint64_t clk_c0 = clk_cta ? clock64() : 0ull;
+  const uint64_t clk_t0 = clk_cta ? ptx::globaltimer_ns() : 0ull;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -417,7 +427,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     ptx::prefetch_tmap(&tmC);
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar_full(s), 2);  // the A and B producers of the leader
-      ptx::mbar_init(bar_empty(s), Cfg::kMc);  // one tcgen05.commit per pair reading the stage
+      ptx::mbar_init(bar_empty(s), Cfg::kPairs);  // one tcgen05.commit per pair of the cluster
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(bar_tfull(b), 1);
@@ -490,9 +500,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       bool have = sched.next(wi);
       int32_t row = have ? row_of(wi) : 0;
       if (have && ptx::elect_one()) {
-        // (With two pairs per cluster, the second pair's tile may lie wholly
-        // beyond N: its B loads then only fill zeros, nothing to prefetch.)
-        const bool in_range = Cfg::kMc == 1 || is_a || row < args.N;
+        // (With several pairs per cluster, a pair's tile may lie wholly
+        // beyond M or N: its loads then only fill zeros, nothing to prefetch.)
+        const bool in_range = is_a ? row < args.M : row < args.N;
         const int32_t kb_end = !in_range ? wi.kb0 : wi.kb1 < wi.kb0 + S ? wi.kb1 : wi.kb0 + S;
         for (int32_t kb = wi.kb0; kb < kb_end; ++kb) {
           if (mn) {
@@ -608,6 +618,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                             : ptx::sw128_kmajor_desc(sA(stage));
           const uint64_t b_desc = args.b_mn ? ptx::sw128_mnmajor_desc(sB(stage))
                                             : ptx::sw128_kmajor_desc(sB(stage));
+          // K steps holding data: all four, except in a last k-block cut by
+          // K, whose steps past K multiply the zeros the TMA filled in.
+          const int32_t k_steps = kb == args.num_kb - 1 ? (args.K - kb * Cfg::kBK + 15) / 16
+                                                        : Cfg::kBK / 16;
           if (ptx::elect_one()) {
 #pragma unroll
             for (int k = 0; k < Cfg::kBK / 16; ++k) {
@@ -615,11 +629,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               // (K-major) or +16 K-rows = 2048 bytes (MN-major); descriptors
               // count in 16 B.  The first step of the item overwrites the
               // accumulator.
-              ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + a_kstep * k, b_desc + b_kstep * k, idesc,
-                                       (kb != wi.kb0 || k != 0) ? 1u : 0u);
+              if (k < k_steps)
+                ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + a_kstep * k, b_desc + b_kstep * k,
+                                         idesc, (kb != wi.kb0 || k != 0) ? 1u : 0u);
             }
-            // The stage is free once every pair reading it is done: with A
-            // multicast both pairs' issuers release it in all four CTAs.
+            // The stage is free once every pair reading it is done: with
+            // multicast every pair's issuer releases it in every CTA of the
+            // cluster.
             if constexpr (kPair)
               ptx::mma_commit_pair(bar_empty(stage), kClusterMask);
             else
@@ -996,6 +1012,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc<Cfg::kCtas>(tmem_base, Cfg::kTmemCols);
+  }
+  if (clk_cta) {
+    const uint64_t c1 = clock64();
+    const uint64_t t1 = ptx::globaltimer_ns();
+    atomicAdd(args.clk, 1ull);
+    atomicAdd(args.clk + 1, static_cast<unsigned long long>(c1 - clk_c0));
+    atomicAdd(args.clk + 2, static_cast<unsigned long long>(t1 - clk_t0));
   }
 }
 

@@ -80,8 +80,8 @@ typedef enum {
 
 /* Create a plan bound to CUDA device `device` (must be an sm_103 part).
  * Queries the SM count, resolves the tensor-map encoder from the driver, sets
- * the kernels' shared-memory limits and allocates the 16-byte device watchdog
- * record.  *out receives the plan, or NULL on error. */
+ * the kernels' shared-memory limits and allocates a 64-byte device record
+ * (the kernel's watchdog and clock records) and the stream-K workspace.  *out receives the plan, or NULL on error. */
 GEMM_API gemm_status_t gemm_plan_create(gemm_plan_t* out, int device);
 
 /* Release the plan and everything it allocated.  NULL is accepted (no-op).
@@ -90,8 +90,13 @@ GEMM_API gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 
 /* C = A x B^T on device buffers, asynchronously on `stream` (a cudaStream_t
  * of the plan's device; NULL = legacy default stream).  A, B and C must be
- * memory of the plan's device: the library does not look the pointers up,
- * and the kernel would fault on another GPU's memory.
+ * device memory of the plan's device (cudaMalloc, cudaMallocAsync or virtual
+ * memory mapped there): a pointer is looked up with cudaPointerGetAttributes
+ * the first time the plan sees it with a given shape (the plan caches the
+ * tensor map it then builds), and host, managed or unregistered memory, or
+ * another GPU's memory, is refused with GEMM_ERR_INVALID_ARG before any
+ * launch.  (Memory freed and allocated again at the same address is not
+ * looked up again while its map stays in the plan's 32-entry cache.)
  *   A : device pointer, fp16 [M, K] row-major (K contiguous), 16-byte aligned
  *   B : device pointer, fp16 [N, K] row-major (K contiguous), 16-byte aligned
  *   C : device pointer, fp16 [M, N] row-major, 16-byte aligned, must not
@@ -111,7 +116,8 @@ GEMM_API gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, 
 /* gemm_run with a choice of storage for each operand (see gemm_layout_t).
  * Alignment rules: N % 8 == 0 always (rows of C); K % 8 == 0 if either
  * operand is K-contiguous; M % 8 == 0 if A is M-contiguous; pointers 16-byte
- * aligned.  Otherwise as gemm_run (asynchronous, allocates nothing). */
+ * aligned.  Otherwise as gemm_run (device memory of the plan's device,
+ * asynchronous, allocates nothing). */
 GEMM_API gemm_status_t gemm_run_ex(gemm_plan_t plan, const void* A, gemm_layout_t layout_a,
                                    const void* B, gemm_layout_t layout_b, void* C,
                                    int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
@@ -142,6 +148,18 @@ GEMM_API gemm_status_t gemm_plan_check_error(gemm_plan_t plan);
  * detail[0] = status code, detail[1] = which wait gave up (see the kernel's
  * WaitSite list), detail[2] = CTA index, detail[3] = tile index. */
 GEMM_API gemm_status_t gemm_plan_last_error_detail(gemm_plan_t plan, uint32_t detail[4]);
+
+/* The SM clock the kernels actually ran at.  Every GEMM kernel launched
+ * through the plan has its first CTA add 1, its lifetime in SM cycles
+ * (%clock64) and its lifetime in nanoseconds (%globaltimer) to a device
+ * record; this call synchronizes the device, copies the record to
+ * out[0] = launches, out[1] = cycles, out[2] = ns, and sets it back to
+ * zero.  out[1] * 1000 / out[2] is the mean SM clock in MHz over those
+ * launches (a clock sampled from outside, e.g. by NVML, can miss the drop a
+ * power-capped kernel causes).  gemm_run_host's launches count too; the
+ * K == 0 zero-fill does not.  No counterpart in the source pages (a
+ * measurement aid). */
+GEMM_API gemm_status_t gemm_plan_kernel_clock(gemm_plan_t plan, uint64_t out[3]);
 
 /* Watchdog and fault-injection controls (testing and diagnosis).
  * timeout_ns: how long any one wait inside the kernel may take before it
@@ -194,6 +212,18 @@ GEMM_API gemm_status_t gemm_plan_set_variant(gemm_plan_t plan, int32_t variant);
 GEMM_API int32_t gemm_variant_count(void);
 GEMM_API const char* gemm_variant_name(int32_t variant);
 
+/* Shape of a variant's unit of work: out[0] CTAs per unit (1, 2 or 4: a
+ * CTA, a CTA pair, or a cluster of two pairs), out[1] x out[2] the
+ * tile of C one unit owns (rows x columns), out[3] 1 if the MMA roles are
+ * swapped (tiles then run over C's columns first).  Returns 0, or -1 for an
+ * unknown variant. */
+GEMM_API int32_t gemm_variant_info(int32_t variant, int32_t out[4]);
+
+/* How many units of each kind fit on the plan's device at once: out[0]
+ * SMs (one-CTA units), out[1] CTA pairs, out[2] clusters of two pairs
+ * (each CTA takes one SM). */
+GEMM_API gemm_status_t gemm_plan_resident_units(gemm_plan_t plan, int32_t out[3]);
+
 /* The variant gemm_run would use for this shape and accumulation, and the
  * grid it would launch (CTAs), or -1 on a rejected shape. */
 GEMM_API int32_t gemm_plan_pick_variant(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
@@ -203,9 +233,12 @@ GEMM_API int32_t gemm_plan_pick_variant(gemm_plan_t plan, int64_t M, int64_t N, 
  * gemm_run_host; the K == 0 zero-fill counts as one). */
 GEMM_API uint64_t gemm_plan_launch_count(gemm_plan_t plan);
 
-/* C = A x B^T exactly as gemm_run computes it, for callers that cannot
- * allocate device memory: no plan, and no cudaMalloc, cudaFree or allocating
- * library call anywhere in the call.  Who needs it: code running under an
+/* C = A x B^T for callers that cannot allocate device memory: no plan, and
+ * no cudaMalloc, cudaFree or allocating library call anywhere in the call.
+ * It always runs the one-CTA kernel (tc_single_128x256_s4) on whole tiles:
+ * the same sum of the same products, but gemm_run may pick another tile
+ * shape or split a tile's k-blocks over several SMs for the same shape, so
+ * the two agree within the accumulation's tolerance, not bit for bit.  Who needs it: code running under an
  * allocator that owns all device memory (a framework's caching allocator or a
  * fixed arena, where a stray cudaMalloc can fail or fragment the pool), and
  * latency-bound loops that cannot afford cudaMalloc's implicit device
@@ -213,7 +246,9 @@ GEMM_API uint64_t gemm_plan_launch_count(gemm_plan_t plan);
  * exists for those callers only.
  *
  * Arguments, layouts, shape and alignment rules, and the K == 0 / empty
- * cases are those of gemm_run; the device is the caller's current device.
+ * cases are those of gemm_run; the device is the caller's current device,
+ * and A, B and C must be device memory of that device (checked as in
+ * gemm_run).
  * The kernel's only scratch (its 16-byte watchdog record) lives in a static
  * 256-byte device array inside the library, which every GPU that loads the
  * library holds until the process exits; a call whose scratch would not fit

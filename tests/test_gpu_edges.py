@@ -56,6 +56,45 @@ def test_rejected_arguments_write_nothing(plan):
     assert bool((c == 3.0).all())
 
 
+def test_memory_of_no_device_or_the_host_is_refused(plan):
+    """A, B and C must be device memory of the plan's device: host memory,
+    pinned or pageable, is refused before any launch."""
+    a = torch.ones((64, 64), dtype=torch.float16, device="cuda")
+    c = torch.full((64, 64), 3.0, dtype=torch.float16, device="cuda")
+    pinned = torch.ones((64, 64), dtype=torch.float16).pin_memory()
+    pageable = np.ones((64, 64), dtype=np.float16)
+    before = plan.launch_count
+    for ha in (pinned.data_ptr(), pageable.ctypes.data):
+        assert plan.status_run(ha, a.data_ptr(), c.data_ptr(), 64, 64, 64) == INVALID
+        assert plan.status_run(a.data_ptr(), ha, c.data_ptr(), 64, 64, 64) == INVALID
+        assert plan.status_run(a.data_ptr(), a.data_ptr(), ha, 64, 64, 64) == INVALID
+        assert plan.status_run(0, 0, ha, 64, 64, 0) == INVALID       # K == 0 writes C
+        st = plan._lib.gemm_run_ex(plan._h, ha, 1, a.data_ptr(), 0, c.data_ptr(), 64, 64, 64,
+                                   0, torch.cuda.current_stream().cuda_stream)
+        assert st == INVALID
+    torch.cuda.synchronize()
+    assert plan.launch_count == before
+    assert bool((c == 3.0).all())
+
+
+def test_kernel_clock_record(plan):
+    """Each GEMM launch adds one to the kernel's clock record, with CTA 0's
+    lifetime in SM cycles and ns: their ratio is an SM clock the part can
+    run at, and reading the record clears it."""
+    M = N = K = 1024
+    a, b = wl.draw(M, N, K, seed=33)
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    c = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    plan.kernel_clock()
+    for _ in range(5):
+        plan.run(ta, tb, c)
+    r = plan.kernel_clock()
+    assert r["launches"] == 5 and r["cycles"] > 0 and r["ns"] > 0
+    assert 200.0 < r["mhz"] < 3000.0, r
+    assert plan.kernel_clock()["launches"] == 0
+    plan.check_error()
+
+
 def test_writes_stay_inside_C(plan):
     """C sits inside a larger buffer of sentinels; a ragged shape must leave
     every byte before and after it untouched."""

@@ -25,9 +25,10 @@ PAIR = "tc_pair_256x256_s6"
 
 # (M, N, K): the ragged workload; an odd number of 256-column tiles (the
 # second pair of the last unit has no columns of C); one k-block; a single
-# unit tile; several tile-rows with a ragged K tail.
+# unit tile; several tile-rows with a ragged K tail; fewer rows than one
+# tile with a last k-block of 8 (one of its four 16-deep MMA steps used).
 SHAPES = [(3000, 5000, 4104), (600, 1280, 520), (300, 760, 64), (256, 512, 1024),
-          (1100, 2056, 2056)]
+          (1100, 2056, 2056), (200, 520, 1032)]
 
 
 def _plan(variant, schedule):
@@ -125,6 +126,8 @@ def test_automatic_choice(plan):
 def test_describe_reports_two_pair_clusters():
     p = _plan(MC, "auto")
     d = p.describe(3000, 5000, 4104)
+    units = p.resident_units()
     p.close()
     assert d["variant"] == MC
-    assert d["grid_ctas"] == 4 * d["units"] and d["units"] >= 1
+    assert d["grid_ctas"] == 4 * d["units"] and 1 <= d["units"] <= units["quads"]
+    assert g.variant_info(MC) == {"ctas": 4, "tile_m": 256, "tile_n": 512, "swap": False}
