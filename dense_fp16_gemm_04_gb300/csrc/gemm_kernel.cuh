@@ -923,60 +923,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (*last_flag == 0u) continue;
         __threadfence();
       }
-#pragma unroll 1
-      for (int c = 0; c < Cfg::kBN / 64; ++c) {
-        uint32_t packed[32];
-        if (split) {
-          // (c) The tile's value: the contributors' partials summed in unit
-          // order, so the result does not depend on who finished last.
-          float acc[64];
-#pragma unroll
-          for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-          for (int32_t j = 0; j < wi.splits; ++j) {
-            const int32_t u = wi.first_unit + j;
-            const float* src = partial(u, sched.slot_of(u, wi.sk_tile)) +
-                               static_cast<size_t>(row_in_cta) * 4 +
-                               static_cast<size_t>(c * 16) * (Cfg::kBM * 4);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float4 v = ptx::ld_global_cg_v4(src + static_cast<size_t>(i) * (Cfg::kBM * 4));
-              acc[4 * i] += v.x;
-              acc[4 * i + 1] += v.y;
-              acc[4 * i + 2] += v.z;
-              acc[4 * i + 3] += v.w;
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) packed[i] = pack_half2(acc[2 * i], acc[2 * i + 1]);
-        } else {
-          if constexpr (Cfg::kAccF16) {
-            ptx::tmem_ld_32x32b_x32_pack16(t_row + c * 64, packed);
-            ptx::tmem_wait_ld(packed);
-          } else {
-            uint32_t v0[32], v1[32];
-            ptx::tmem_ld_32x32b_x32(t_row + c * 64, v0);
-            ptx::tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
-            ptx::tmem_wait_ld(v0);
-            ptx::tmem_regs_ready(v1);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              packed[i] = pack_half2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
-              packed[16 + i] =
-                  pack_half2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
-            }
-          }
-          if (c == Cfg::kBN / 64 - 1) {
-            // The whole accumulator buffer is in registers: hand it back.
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (kPair)
-                ptx::mbar_arrive_cluster(tempty_bar0 + 8u * buf);
-              else
-                ptx::mbar_arrive(tempty_bar0 + 8u * buf);
-            }
-          }
-        }
+      // Stage one 32 x 64 chunk of fp16 C through this warp's swizzled
+      // shared-memory buffers and store it with the TMA engine.
+      auto store_chunk = [&](const uint32_t (&packed)[32], int c) {
         const uint32_t sbuf = stage_base + (stores & 1u) * Cfg::kEpiBufBytes;
         if (stores >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();
         __syncwarp();
@@ -998,6 +947,80 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           ++stores;
         }
         stores = __shfl_sync(0xffffffffu, stores, 0);
+      };
+      // The whole accumulator buffer is in registers: hand it back.
+      auto release_tmem = [&]() {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair)
+            ptx::mbar_arrive_cluster(tempty_bar0 + 8u * buf);
+          else
+            ptx::mbar_arrive(tempty_bar0 + 8u * buf);
+        }
+      };
+      if (split) {
+#pragma unroll 1
+        for (int c = 0; c < Cfg::kBN / 64; ++c) {
+          // (c) The tile's value: the contributors' partials summed in unit
+          // order, so the result does not depend on who finished last.
+          float acc[64];
+#pragma unroll
+          for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+          for (int32_t j = 0; j < wi.splits; ++j) {
+            const int32_t u = wi.first_unit + j;
+            const float* src = partial(u, sched.slot_of(u, wi.sk_tile)) +
+                               static_cast<size_t>(row_in_cta) * 4 +
+                               static_cast<size_t>(c * 16) * (Cfg::kBM * 4);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float4 v = ptx::ld_global_cg_v4(src + static_cast<size_t>(i) * (Cfg::kBM * 4));
+              acc[4 * i] += v.x;
+              acc[4 * i + 1] += v.y;
+              acc[4 * i + 2] += v.z;
+              acc[4 * i + 3] += v.w;
+            }
+          }
+          uint32_t packed[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) packed[i] = pack_half2(acc[2 * i], acc[2 * i + 1]);
+          store_chunk(packed, c);
+        }
+      } else if constexpr (Cfg::kAccF16) {
+#pragma unroll 1
+        for (int c = 0; c < Cfg::kBN / 64; ++c) {
+          uint32_t packed[32];
+          ptx::tmem_ld_32x32b_x32_pack16(t_row + c * 64, packed);
+          ptx::tmem_wait_ld(packed);
+          if (c == Cfg::kBN / 64 - 1) release_tmem();
+          store_chunk(packed, c);
+        }
+      } else {
+        // fp32 accumulator: the TMEM loads of chunk c + 1 are issued as soon
+        // as chunk c is packed, so they run while chunk c is staged and
+        // stored.
+        uint32_t v0[32], v1[32];
+        ptx::tmem_ld_32x32b_x32(t_row, v0);
+        ptx::tmem_ld_32x32b_x32(t_row + 32, v1);
+#pragma unroll 1
+        for (int c = 0; c < Cfg::kBN / 64; ++c) {
+          uint32_t packed[32];
+          ptx::tmem_wait_ld(v0);
+          ptx::tmem_regs_ready(v1);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            packed[i] = pack_half2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+            packed[16 + i] = pack_half2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+          }
+          ptx::tmem_regs_ready(packed);  // packed before v0 and v1 are loaded again
+          if (c + 1 < Cfg::kBN / 64) {
+            ptx::tmem_ld_32x32b_x32(t_row + (c + 1) * 64, v0);
+            ptx::tmem_ld_32x32b_x32(t_row + (c + 1) * 64 + 32, v1);
+          } else {
+            release_tmem();
+          }
+          store_chunk(packed, c);
+        }
       }
     }
     if (lane == 0) ptx::bulk_wait_group<0>();
