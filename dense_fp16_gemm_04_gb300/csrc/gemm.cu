@@ -47,6 +47,12 @@ using Swap64F16 = GemmCfg<1, 8, true, 64, true>;
 // Two CTA pairs per cluster sharing the A block of their tile-row (multicast).
 using PairMcF32 = GemmCfg<2, 6, false, 256, false, 2>;
 using PairMcF16 = GemmCfg<2, 6, true, 256, false, 2>;
+// Split-K clusters (fp32 accumulation only): the CTAs of a cluster share each
+// tile, one k-slice each, and add their partials through shared memory.
+using Swap16K2F32 = GemmCfg<1, 11, false, 16, true, 1, 2>;
+using Swap32K2F32 = GemmCfg<1, 10, false, 32, true, 1, 2>;
+using Swap64K2F32 = GemmCfg<1, 8, false, 64, true, 1, 2>;
+using Single64K4F32 = GemmCfg<1, 4, false, 64, false, 1, 4>;
 
 struct VariantInfo {
   const char* name;
@@ -56,6 +62,8 @@ struct VariantInfo {
   int box_a_rows;      // rows of A each CTA loads per stage (K-contiguous A)
   int box_b_rows;      // rows of B each CTA loads per stage
   bool swap;           // MMA roles swapped: the kernel's tiles run over (N, M)
+  int ksplit;          // CTAs of a split-K cluster sharing each tile (1: none)
+  int base;            // the variant with whole tiles per CTA it refines (itself if none)
 };
 
 constexpr int kVariantPair = 0;
@@ -66,16 +74,24 @@ constexpr int kVariantSwap16 = 4;
 constexpr int kVariantSwap32 = 5;
 constexpr int kVariantSwap64 = 6;
 constexpr int kVariantPairMc = 7;
-constexpr int kNumVariants = 8;
+constexpr int kVariantSwap16K2 = 8;
+constexpr int kVariantSwap32K2 = 9;
+constexpr int kVariantSwap64K2 = 10;
+constexpr int kVariantSingle64K4 = 11;
+constexpr int kNumVariants = 12;
 constexpr VariantInfo kVariants[kNumVariants] = {
-    {"tc_pair_256x256_s6", 2, 256, 256, 128, 128, false},
-    {"tc_single_128x256_s4", 1, 128, 256, 128, 256, false},
-    {"tc_pair_256x128_s8", 2, 256, 128, 128, 64, false},
-    {"tc_single_128x64_s8", 1, 128, 64, 128, 64, false},
-    {"tc_swap_16x128_s11", 1, 16, 128, 16, 128, true},
-    {"tc_swap_32x128_s10", 1, 32, 128, 32, 128, true},
-    {"tc_swap_64x128_s8", 1, 64, 128, 64, 128, true},
-    {"tc_pair_mc_256x256_s6", 4, 256, 512, 64, 128, false},
+    {"tc_pair_256x256_s6", 2, 256, 256, 128, 128, false, 1, 0},
+    {"tc_single_128x256_s4", 1, 128, 256, 128, 256, false, 1, 1},
+    {"tc_pair_256x128_s8", 2, 256, 128, 128, 64, false, 1, 2},
+    {"tc_single_128x64_s8", 1, 128, 64, 128, 64, false, 1, 3},
+    {"tc_swap_16x128_s11", 1, 16, 128, 16, 128, true, 1, 4},
+    {"tc_swap_32x128_s10", 1, 32, 128, 32, 128, true, 1, 5},
+    {"tc_swap_64x128_s8", 1, 64, 128, 64, 128, true, 1, 6},
+    {"tc_pair_mc_256x256_s6", 4, 256, 512, 64, 128, false, 1, 7},
+    {"tc_swap_16x128_k2", 2, 16, 128, 16, 128, true, 2, kVariantSwap16},
+    {"tc_swap_32x128_k2", 2, 32, 128, 32, 128, true, 2, kVariantSwap32},
+    {"tc_swap_64x128_k2", 2, 64, 128, 64, 128, true, 2, kVariantSwap64},
+    {"tc_single_128x64_k4", 4, 128, 64, 128, 64, false, 4, kVariantSingle64},
 };
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s for any single wait
@@ -103,6 +119,7 @@ struct gemm_plan_s {
   int num_sms = 0;
   int max_pairs = 0;  // CTA pairs of the pair kernel that fit on the device at once
   int max_quads = 0;  // two-pair clusters of the multicast kernel that fit at once
+  int max_units[kNumVariants] = {};  // units (CTAs or clusters) of each variant that fit at once
   // Stream-K workspace, allocated once at plan creation: partial fp32 tiles
   // (2 slots per unit) and per-tile contribution counters (kept at zero
   // between launches by the kernel itself).
@@ -286,6 +303,32 @@ int auto_variant(int64_t M, int64_t N, int64_t K, bool k_major, int max_pairs, i
   return kVariantPair;
 }
 
+// The split-K cluster variant to use instead of variant v for T tiles of KB
+// k-blocks, or -1.  With swapped roles, when every tile would be cut into
+// exactly two k-pieces (T <= U / 2), a cluster of two CTAs per tile adds the
+// second piece's partial through shared memory, instead of parking both in
+// global memory and counting them (64 x 8192^2 +8%, 16 and 32 x 8192^2 +7%,
+// alternating runs on GB300).  A problem of few 128 x 64 tiles (T at most a
+// quarter of the SMs) with at least 8 k-blocks per CTA takes four CTAs per
+// tile, so that each CTA loads a quarter of the tile's operands
+// (128 x 1024 x 8192 2.4x, 256 x 256 x 4096 1.8x); with fewer (512^3: 2 per
+// CTA) launching the four-CTA clusters costs more than it saves (-22%).
+int split_k_variant(int v, int64_t T, int64_t KB, const int* max_units) {
+  int ks = -1;
+  if (kVariants[v].swap && kVariants[v].ksplit == 1) {
+    const int64_t U = max_units[v];
+    const int64_t pieces = T > 0 ? std::min<int64_t>(U / T, KB / kMinSkIters) : 0;
+    const bool cut = T < U && (kVariants[v].tile_m >= 32 || 2 * T <= U);
+    if (cut && pieces == 2)
+      ks = v == kVariantSwap16 ? kVariantSwap16K2 : v == kVariantSwap32 ? kVariantSwap32K2
+                                                                         : kVariantSwap64K2;
+  } else if (v == kVariantSingle64) {
+    if (4 * T <= max_units[kVariantSingle64] && KB >= 4 * 8) ks = kVariantSingle64K4;
+  }
+  if (ks >= 0 && (T > max_units[ks] || KB < kVariants[ks].ksplit)) ks = -1;
+  return ks;
+}
+
 // `mn`: an operand is stored M- or N-contiguous (the swapped-roles variants
 // take K-contiguous operands only).
 Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, gemm_acc_t acc,
@@ -293,14 +336,23 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
   int v = p->forced_variant >= 0 ? p->forced_variant
                                  : auto_variant(M, N, K, !mn, p->max_pairs, p->max_quads);
   if (mn && kVariants[v].swap) v = M <= 128 ? kVariantSingle64 : kVariantPair;
+  const int64_t KB = (K + 63) / 64;
+  // Split-K clusters take fp32 accumulation and at least one k-block per CTA.
+  if (kVariants[v].ksplit > 1 && (acc != GEMM_ACC_F32 || KB < kVariants[v].ksplit))
+    v = kVariants[v].base;
   if (kVariants[v].ctas == 4 && p->max_quads < 1) v = kVariantPair;
   if (kVariants[v].ctas == 2 && p->max_pairs < 1) v = kVariantSingle;
+  if (p->max_units[v] < 1) v = kVariants[v].base;
+  // Automatic choice of a split-K cluster: few tiles, each with many
+  // k-blocks, spread over the SMs by cutting K instead of sharing partial
+  // tiles through global memory (see split_k_variant).
+  if (p->forced_variant < 0 && p->schedule_mode == 0 && acc == GEMM_ACC_F32) {
+    const int ks = split_k_variant(v, tiles_of(kVariants[v], M, N), KB, p->max_units);
+    if (ks >= 0) v = ks;
+  }
   const VariantInfo& vi = kVariants[v];
   const int64_t T = tiles_of(vi, M, N);
-  const int64_t KB = (K + 63) / 64;
-  const int64_t U = vi.ctas == 4   ? p->max_quads
-                    : vi.ctas == 2 ? p->max_pairs
-                                   : p->num_sms;
+  const int64_t U = p->max_units[v];
   Schedule s;
   s.variant = v;
   s.units = T < U ? T : U;
@@ -315,7 +367,7 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
   // share is cheap even with no whole tiles after it: it is what spreads a
   // few tall tiles over every SM.
   const bool allowed = acc == GEMM_ACC_F32 && p->sk_ws && p->sk_count && KB > 0 &&
-                       p->schedule_mode != 1 &&
+                       p->schedule_mode != 1 && vi.ksplit == 1 &&
                        ((T % U != 0 && (T >= U || vi.swap)) || p->schedule_mode == 2);
   if (allowed) {
     // Only the tiles of the part-empty last wave are shared (all tiles when
@@ -369,7 +421,7 @@ Schedule make_schedule(const gemm_plan_s* p, int64_t M, int64_t N, int64_t K, ge
   // Its hand-off costs ~0.5% when the clock is not capped (8192^3: 1908 vs
   // 1898 TFLOP/s, 13 waves), so it is used from 24 waves of whole tiles on.
   // (Mode 2, for testing, uses the machinery whenever there are whole tiles.)
-  s.dyn = p->tile_ctr != nullptr && p->tile_order != 1 &&
+  s.dyn = p->tile_ctr != nullptr && p->tile_order != 1 && vi.ksplit == 1 &&
           (p->tile_order == 2 ? s.dp_tiles > 0 : s.dp_tiles >= 24 * s.units);
   s.grid = static_cast<int>(s.units * vi.ctas);
   return s;
@@ -521,6 +573,19 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
       e = f32 ? launch_gemm<Swap64F32>(ma, mb, mc, args, grid, stream, p->pdl)
               : launch_gemm<Swap64F16>(ma, mb, mc, args, grid, stream, p->pdl);
       break;
+    // Split-K clusters: fp32 only (make_schedule never picks them for fp16).
+    case kVariantSwap16K2:
+      e = launch_gemm<Swap16K2F32>(ma, mb, mc, args, grid, stream, p->pdl);
+      break;
+    case kVariantSwap32K2:
+      e = launch_gemm<Swap32K2F32>(ma, mb, mc, args, grid, stream, p->pdl);
+      break;
+    case kVariantSwap64K2:
+      e = launch_gemm<Swap64K2F32>(ma, mb, mc, args, grid, stream, p->pdl);
+      break;
+    case kVariantSingle64K4:
+      e = launch_gemm<Single64K4F32>(ma, mb, mc, args, grid, stream, p->pdl);
+      break;
     default:
       e = f32 ? launch_gemm<SingleF32>(ma, mb, mc, args, grid, stream, p->pdl)
               : launch_gemm<SingleF16>(ma, mb, mc, args, grid, stream, p->pdl);
@@ -626,7 +691,9 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
       set_smem_attr<Swap16F32>() != cudaSuccess || set_smem_attr<Swap16F16>() != cudaSuccess ||
       set_smem_attr<Swap32F32>() != cudaSuccess || set_smem_attr<Swap32F16>() != cudaSuccess ||
       set_smem_attr<Swap64F32>() != cudaSuccess || set_smem_attr<Swap64F16>() != cudaSuccess ||
-      set_smem_attr<PairMcF32>() != cudaSuccess || set_smem_attr<PairMcF16>() != cudaSuccess) {
+      set_smem_attr<PairMcF32>() != cudaSuccess || set_smem_attr<PairMcF16>() != cudaSuccess ||
+      set_smem_attr<Swap16K2F32>() != cudaSuccess || set_smem_attr<Swap32K2F32>() != cudaSuccess ||
+      set_smem_attr<Swap64K2F32>() != cudaSuccess || set_smem_attr<Single64K4F32>() != cudaSuccess) {
     delete p;
     return GEMM_ERR_CUDA;
   }
@@ -638,6 +705,14 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     p->max_pairs = m;
     const int q0 = max_active_clusters<PairMcF32>(), q1 = max_active_clusters<PairMcF16>();
     p->max_quads = q0 < q1 ? q0 : q1;
+    for (int v = 0; v < kNumVariants; ++v) {
+      const int c = kVariants[v].ctas;
+      p->max_units[v] = c == 4 ? p->max_quads : c == 2 ? p->max_pairs : p->num_sms;
+    }
+    p->max_units[kVariantSwap16K2] = max_active_clusters<Swap16K2F32>();
+    p->max_units[kVariantSwap32K2] = max_active_clusters<Swap32K2F32>();
+    p->max_units[kVariantSwap64K2] = max_active_clusters<Swap64K2F32>();
+    p->max_units[kVariantSingle64K4] = max_active_clusters<Single64K4F32>();
   }
   // 16-byte watchdog record, then three 8-byte clock counters.
   if (cudaMalloc(&p->d_err, kRecordBytes) != cudaSuccess) {

@@ -3,7 +3,7 @@
 //   C[M,N] = A[M,K] x B[N,K]^T, fp16 in, fp32 or fp16 accumulate, fp16 out
 //   (tilus "A Minimal Hopper Matmul", section "Block Tiling").
 //
-// One template, four forms:
+// One template, five forms:
 //   kCtas = 1           one CTA per SM owns a 128 x kBN tile of C (kBN = 64..256);
 //   kCtas = 2           a cluster of two CTAs on neighbouring SMs owns a
 //                       256 x kBN tile: each CTA loads its 128 rows of A and
@@ -19,7 +19,16 @@
 //   kSwap               roles swapped for C with few rows: the MMA's M runs
 //                       over 128 columns of C (rows of B) and its N over
 //                       kBN = 16..64 rows of C, and the epilogue writes the
-//                       transposed tile straight to C.
+//                       transposed tile straight to C;
+//   kSplit = 2 or 4     a cluster of single CTAs (plain or swapped roles)
+//                       shares every tile it is given, each CTA accumulating
+//                       one k-slice; the CTAs of rank > 0 write their fp32
+//                       partial tiles into rank 0's shared memory
+//                       (st.shared::cluster, one release arrival per thread)
+//                       and rank 0 adds them to its own, in rank order, and
+//                       stores the tile -- for problems of few tiles with many
+//                       k-blocks each, without a round trip through global
+//                       memory.
 // Operands are K-contiguous or M/N-contiguous (run-time choice: TMA box shape,
 // shared-memory descriptor and the instruction descriptor's transpose bits).
 //
@@ -75,6 +84,8 @@ enum WaitSite : uint32_t {
   kSiteDrain = 6,      // teardown: producer waiting for its last stages
   kSiteTileFull = 7,   // a role waiting for the next tile from the tile scheduler
   kSiteTileEmpty = 8,  // the tile scheduler waiting for a free slot of its ring
+  kSiteRedFull = 9,    // split-K leader waiting for the other CTAs' partial tiles
+  kSiteRedEmpty = 10,  // split-K CTA waiting for the leader to free its partial slot
 };
 
 constexpr uint32_t kStatusTimeout = 5;  // == GEMM_ERR_TIMEOUT
@@ -194,6 +205,7 @@ struct TileRing {
 // apart (operands then stay in L2 between their uses by neighbouring tiles).
 struct Sched {
   int32_t unit, units, dp_tiles, num_kb, sk_units;
+  int32_t kslice, kslices;  // split-K clusters: this CTA's k-slice of every tile, of kslices
   int64_t sk_iters;
   int32_t next_dp;
   int64_t x, x_end;  // this unit's remaining range of tail k-blocks
@@ -203,9 +215,11 @@ struct Sched {
   TileRing ring;
 
   __device__ __forceinline__ Sched(const GemmArgs& a, int32_t unit_, int32_t units_,
-                                   const TileRing& ring_ = TileRing{})
+                                   const TileRing& ring_ = TileRing{}, int32_t kslice_ = 0,
+                                   int32_t kslices_ = 1)
       : unit(unit_), units(units_), dp_tiles(a.dp_tiles), num_kb(a.num_kb),
-        sk_units(a.sk_units), sk_iters(a.sk_iters), next_dp(unit_), x(0), x_end(0),
+        sk_units(a.sk_units), kslice(kslice_), kslices(kslices_), sk_iters(a.sk_iters),
+        next_dp(unit_), x(0), x_end(0),
         dyn(a.tile_ctr != nullptr), first_done(false), n(0), ring(ring_) {
     if (sk_units > 0 && unit < sk_units) {
       x = bound(unit);
@@ -232,12 +246,14 @@ struct Sched {
     }
     return static_cast<int32_t>(v);
   }
+  // A whole tile; in a split-K cluster, this CTA's k-slice of it (the
+  // slices of a tile's kslices CTAs partition its k-blocks, each non-empty).
   __device__ __forceinline__ void whole(WorkItem& w, int32_t t) const {
     w.tile = t;
-    w.kb0 = 0;
-    w.kb1 = num_kb;
+    w.kb0 = kslice * num_kb / kslices;
+    w.kb1 = (kslice + 1) * num_kb / kslices;
     w.sk_tile = -1;
-    w.splits = 1;
+    w.splits = kslices;
     w.first_unit = unit;
   }
   // First tail k-block of unit u.
@@ -287,7 +303,7 @@ struct Sched {
 
 // Tile configuration.  kCtas CTAs cooperate on one tile of kTileM x kBN.
 template <int kCtas_, int kStages_, bool kAccF16_, int kBN_ = 256, bool kSwap_ = false,
-          int kMc_ = 1>
+          int kMc_ = 1, int kSplit_ = 1>
 struct GemmCfg {
   static constexpr int kCtas = kCtas_;
   // kMc = 2: a cluster holds two CTA pairs working on neighbouring tiles of
@@ -296,7 +312,12 @@ struct GemmCfg {
   // position of the other pair, so every SM requests half as many A bytes.
   static constexpr int kMc = kMc_;
   static constexpr int kPairs = kMc;  // CTA pairs (or lone CTAs) per cluster
-  static constexpr int kClusterCtas = kCtas * kPairs;
+  // kSplit > 1: a cluster of kSplit single CTAs shares every tile it is
+  // given, each CTA accumulating its own k-slice; the CTAs of rank > 0 write
+  // their fp32 partial tiles into the shared memory of rank 0, which adds
+  // them to its own (in rank order) and stores the tile.
+  static constexpr int kSplit = kSplit_;
+  static constexpr int kClusterCtas = kCtas * kPairs * kSplit;
   // Swapped roles (for small M): the MMA's "A" operand is a 128-row tile of B
   // and its "B" operand a kBN-row tile of A, so D = tile of C^T.
   static constexpr bool kSwap = kSwap_;
@@ -314,13 +335,17 @@ struct GemmCfg {
   static constexpr int kEpiWarps = 4;
   static constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 fp16, 128B swizzle
   static constexpr int kEpiBytes = kSwap ? 0 : kEpiWarps * 2 * kEpiBufBytes;
+  // Split-K: kSplit - 1 partial tiles of 128 x kBN fp32 received by rank 0,
+  // each stored [column / 4][row][column % 4].
+  static constexpr int kRedBytes = (kSplit - 1) * kBM * kBN * 4;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kStages * kABytes;
   static constexpr int kOffEpi = kStages * kStageBytes;
-  static constexpr int kOffBar = kOffEpi + kEpiBytes;
+  static constexpr int kOffRed = kOffEpi + kEpiBytes;
+  static constexpr int kOffBar = kOffRed + kRedBytes;
   // full, empty, tmem_full[2], tmem_empty[2], mma_done, tile_full[2], tile_empty[2],
-  // tile_took
-  static constexpr int kNumBars = 2 * kStages + 10;
+  // tile_took, red_full, red_empty
+  static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kOffSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffSlot + 4;
   static constexpr int kOffFlag = kOffAbort + 4;           // stream-K "last contributor" flag
@@ -340,6 +365,8 @@ struct GemmCfg {
   static_assert(kMc == 1 || (kMc == 2 && kCtas == 2 && !kSwap),
                 "A multicast between two CTA pairs only");
   static_assert(kClusterCtas <= 8, "portable cluster size");
+  static_assert(kSplit == 1 || ((kSplit == 2 || kSplit == 4) && kCtas == 1 && kMc == 1 && !kAccF16),
+                "split-K clusters: 2 or 4 single CTAs, fp32 partials");
   static_assert(kSwap ? (kCtas == 1 && (kBN == 16 || kBN == 32 || kBN == 64))
                       : (kBN == 64 || kBN == 128 || kBN == 256),
                 "tile width: 64, 128 or 256; 16, 32 or 64 with swapped roles (one CTA)");
@@ -351,7 +378,7 @@ struct GemmCfg {
   // Barriers sit after every TMA destination, never inside one (tilus "A
   // Minimal Hopper Matmul", Epilogue note: a barrier placed inside a live TMA
   // destination is silently corrupted).
-  static_assert(kOffBar >= kOffEpi + kEpiBytes, "barriers overlap a TMA buffer");
+  static_assert(kOffBar >= kOffRed + kRedBytes, "barriers overlap a TMA or partial buffer");
 };
 
 // Grouped raster: tiles are walked down a group of `group` tile-rows before
@@ -379,6 +406,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   constexpr int S = Cfg::kStages;
   constexpr bool kPair = Cfg::kCtas == 2;
+  constexpr bool kSplitK = Cfg::kSplit > 1;
+  constexpr bool kClustered = Cfg::kClusterCtas > 1;
   // CTA 0's start, for the clock record.
   const bool clk_cta = args.clk != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
   const uint64_t clk_c0 = clk_cta ? clock64() : 0ull;
@@ -391,16 +420,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const int lane = threadIdx.x & 31;
   // Position of this CTA in its cluster, in its pair, and of the pair in the
   // cluster; units (CTAs, pairs or two-pair clusters) in the grid.
-  const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
-  const uint32_t cta = rank & 1u;       // 0: the pair's leader, which issues the MMAs
-  const uint32_t pair = rank >> 1;      // which pair of a two-pair cluster
-  const uint32_t leader = rank & ~1u;   // cluster rank of this pair's leader
+  const uint32_t rank = kClustered ? ptx::cluster_ctarank() : 0u;
+  const uint32_t krank = kSplitK ? rank : 0u;  // k-slice of a split-K cluster (0: the leader)
+  const uint32_t prank = kPair ? rank : 0u;    // position among the cluster's CTA pairs
+  const uint32_t cta = prank & 1u;      // 0: the pair's leader, which issues the MMAs
+  const uint32_t pair = prank >> 1;     // which pair of a two-pair cluster
+  const uint32_t leader = prank & ~1u;  // cluster rank of this pair's leader
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << Cfg::kClusterCtas) - 1u);
   const uint16_t pair_mask = static_cast<uint16_t>(0x3u << leader);
   // Tile column of this pair's tile, from the unit's tile column.
   auto tile_nb = [&](int32_t nbx) { return nbx * Cfg::kMc + static_cast<int32_t>(pair); };
-  const int32_t unit = kPair ? static_cast<int32_t>(ptx::cluster_id_x()) : static_cast<int32_t>(blockIdx.x);
-  const int32_t units = kPair ? static_cast<int32_t>(ptx::num_clusters_x()) : static_cast<int32_t>(gridDim.x);
+  const int32_t unit = kClustered ? static_cast<int32_t>(ptx::cluster_id_x()) : static_cast<int32_t>(blockIdx.x);
+  const int32_t units = kClustered ? static_cast<int32_t>(ptx::num_clusters_x()) : static_cast<int32_t>(gridDim.x);
 
   const uint32_t bar0 = sb + Cfg::kOffBar;
   auto bar_full = [&](int s) { return bar0 + 8u * s; };
@@ -411,6 +442,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   auto bar_tile_full = [&](int i) { return bar0 + 8u * (2 * S + 5 + i); };
   auto bar_tile_empty = [&](int i) { return bar0 + 8u * (2 * S + 7 + i); };
   const uint32_t bar_tile_took = bar0 + 8u * (2 * S + 9);
+  const uint32_t bar_red_full = bar0 + 8u * (2 * S + 10);   // split-K: in rank 0
+  const uint32_t bar_red_empty = bar0 + 8u * (2 * S + 11);  // split-K: in every rank > 0
   auto sA = [&](int s) { return sb + Cfg::kOffA + s * Cfg::kABytes; };
   auto sB = [&](int s) { return sb + Cfg::kOffB + s * Cfg::kBBytes; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
@@ -420,6 +453,70 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const TileRing ring{sb + Cfg::kOffTiles, bar_tile_full(0),
                       kPair ? ptx::mapa(bar_tile_empty(0), 0) : bar_tile_empty(0), w, kPair,
                       warp == 0 && rank == 0 ? bar_tile_took : 0u};
+  // Split-K partial tiles in rank 0: slot r - 1 for rank r, element (TMEM
+  // lane l, column c) at ((c / 4) * 128 + l) * 16 + (c % 4) * 4 bytes, so a
+  // warp's 32 lanes move 512 contiguous bytes per 16-byte access.
+  constexpr uint32_t kRedSlotBytes = static_cast<uint32_t>(Cfg::kBM * Cfg::kBN * 4);
+  // Epilogue warps of a split-K CTA: rank > 0 writes its accumulator (TMEM
+  // buffer at t_row, this thread's lane `lrow`) into its slot of rank 0
+  // after rank 0 has emptied the slot, hands the TMEM buffer back and
+  // announces the partial with one release arrival per thread.  Returns
+  // false if a wait gave up.
+  auto splitk_push = [&](uint32_t t_row, int lrow, uint32_t red_par, uint32_t tempty_bar,
+                         int32_t tile) -> bool {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0)
+      ok = wait_bar<true>(bar_red_empty, red_par ^ 1u, w, kSiteRedEmpty, tile) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ptx::named_barrier_and(1, 32 * Cfg::kEpiWarps, ok != 0)) return false;
+    const uint32_t dst = ptx::mapa(sb + Cfg::kOffRed + (krank - 1u) * kRedSlotBytes, 0) +
+                         static_cast<uint32_t>(lrow) * 16u;
+#pragma unroll
+    for (int g = 0; g < Cfg::kBN / 16; ++g) {
+      uint32_t v[16];
+      ptx::tmem_ld_32x32b_x16(t_row + g * 16, v);
+      ptx::tmem_wait_ld(v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ptx::st_shared_cluster_v4(dst + static_cast<uint32_t>((g * 4 + j) * Cfg::kBM) * 16u,
+                                  v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(tempty_bar);
+    ptx::mbar_arrive_release_cluster(ptx::mapa(bar_red_full, 0));
+    return true;
+  };
+  // Rank 0: wait until every other rank's partial of this tile has landed.
+  auto splitk_wait_partials = [&](uint32_t red_par, int32_t tile) -> bool {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0)
+      ok = wait_bar<true>(bar_red_full, red_par, w, kSiteRedFull, tile) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    return ptx::named_barrier_and(1, 32 * Cfg::kEpiWarps, ok != 0);
+  };
+  // Rank 0: add the partials' columns [c0, c0 + n) of lane `lrow` to acc, in
+  // rank order.
+  auto splitk_add = [&](float* acc, int c0, int n, int lrow) {
+    for (uint32_t r = 1; r < static_cast<uint32_t>(Cfg::kSplit); ++r) {
+      const uint32_t src = sb + Cfg::kOffRed + (r - 1u) * kRedSlotBytes +
+                           static_cast<uint32_t>(lrow) * 16u;
+#pragma unroll
+      for (int g4 = 0; g4 < n / 4; ++g4) {
+        const float4 p = ptx::ld_shared_v4_f32(
+            src + static_cast<uint32_t>((c0 / 4 + g4) * Cfg::kBM) * 16u);
+        acc[4 * g4] += p.x;
+        acc[4 * g4 + 1] += p.y;
+        acc[4 * g4 + 2] += p.z;
+        acc[4 * g4 + 3] += p.w;
+      }
+    }
+  };
+  // Rank 0, after reading every partial of the tile: free the slots.
+  auto splitk_release_slots = [&]() {
+    for (uint32_t r = 1; r < static_cast<uint32_t>(Cfg::kSplit); ++r)
+      ptx::mbar_arrive_release_cluster(ptx::mapa(bar_red_empty, r));
+  };
 
   if (threadIdx.x == 0) {
     ptx::prefetch_tmap(&tmA);
@@ -439,6 +536,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       ptx::mbar_init(bar_tile_empty(i), Cfg::kTileConsumers);
     }
     ptx::mbar_init(bar_tile_took, 1);  // the leader's A producer read a tile
+    if constexpr (kSplitK) {
+      // One arrival per epilogue thread of every other rank (each releases
+      // its own partial-tile stores), and one per epilogue thread of rank 0
+      // (each has read its rows of the slot).
+      ptx::mbar_init(bar_red_full, 32 * Cfg::kEpiWarps * (Cfg::kSplit - 1));
+      ptx::mbar_init(bar_red_empty, 32 * Cfg::kEpiWarps);
+    }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -447,8 +551,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     ptx::tmem_relinquish<Cfg::kCtas>();
   }
   ptx::tc_fence_before();
-  if constexpr (kPair)
-    ptx::cluster_sync();  // both CTAs' barriers exist before either uses the other's
+  if constexpr (kClustered)
+    ptx::cluster_sync();  // every CTA's barriers exist before any uses another's
   else
     __syncthreads();
   ptx::tc_fence_after();
@@ -489,7 +593,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                           static_cast<int32_t>(pair) * rows
                     : tile_nb(nbx) * Cfg::kBN + static_cast<int32_t>(cta) * Cfg::kBRows;
       };
-      Sched sched(args, unit, units, ring);
+      Sched sched(args, unit, units, ring, static_cast<int32_t>(krank), Cfg::kSplit);
       WorkItem wi;
       // The first work item is worked out before the wait for the previous
       // kernel, so that after it only the loads themselves remain.  So is an
@@ -593,7 +697,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                              (args.b_mn ? ptx::kIdescBMnMajor : 0u);
       const uint64_t a_kstep = args.a_mn ? 128u : 2u;
       const uint64_t b_kstep = args.b_mn ? 128u : 2u;
-      Sched sched(args, unit, units, ring);
+      Sched sched(args, unit, units, ring, static_cast<int32_t>(krank), Cfg::kSplit);
       WorkItem wi;
       int stage = 0;
       uint32_t phase = 0;
@@ -736,7 +840,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     auto partial = [&](int32_t u, int32_t slot) {
       return args.sk_ws + static_cast<size_t>(u * 2 + slot) * static_cast<size_t>(Cfg::kPartialFloats);
     };
-    Sched sched(args, unit, units, ring);
+    Sched sched(args, unit, units, ring, static_cast<int32_t>(krank), Cfg::kSplit);
     WorkItem wi;
     int32_t acc_iter = 0;
     // All epilogue warps take the same decision (a failed wait for the next
@@ -756,9 +860,29 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                              static_cast<uint32_t>(buf * Cfg::kBN);
       const int32_t n = mb * Cfg::kBM + row_in_cta;  // column of C
       const int32_t m0 = nb * Cfg::kBN;              // first row of C in this tile
-      const bool split = !Cfg::kAccF16 && wi.splits > 1;
+      const bool split = !Cfg::kAccF16 && !kSplitK && wi.splits > 1;
       float acc[Cfg::kBN];
-      if (split) {
+      if constexpr (kSplitK) {
+        const uint32_t red_par = static_cast<uint32_t>((acc_iter - 1) & 1);
+        if (krank != 0) {
+          if (!splitk_push(t_row, row_in_cta, red_par, tempty_bar0 + 8u * buf, wi.tile)) break;
+          continue;  // rank 0 stores the tile
+        }
+        if (!splitk_wait_partials(red_par, wi.tile)) break;
+#pragma unroll
+        for (int g = 0; g < Cfg::kBN / 16; ++g) {
+          uint32_t v[16];
+          ptx::tmem_ld_32x32b_x16(t_row + g * 16, v);
+          ptx::tmem_wait_ld(v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[g * 16 + i] = __uint_as_float(v[i]);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty_bar0 + 8u * buf);
+        splitk_add(acc, 0, Cfg::kBN, row_in_cta);
+        splitk_release_slots();
+      } else if (split) {
         // Same protocol as the plain epilogue: park the fp32 partial, count,
         // and the last contributor sums all partials in unit order.
         float* own = partial(unit, sched.slot_of(unit, wi.sk_tile)) +
@@ -856,7 +980,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       return args.sk_ws + (static_cast<size_t>(u * 2 + slot) * Cfg::kClusterCtas + rank) *
                               static_cast<size_t>(Cfg::kPartialFloats);
     };
-    Sched sched(args, unit, units, ring);
+    Sched sched(args, unit, units, ring, static_cast<int32_t>(krank), Cfg::kSplit);
     WorkItem wi;
     uint32_t stores = 0;
     int32_t acc_iter = 0;
@@ -879,7 +1003,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * Cfg::kBN);
       const int32_t row0 = mb * Cfg::kTileM + static_cast<int32_t>(cta) * Cfg::kBM + q * 32;
-      const bool split = !Cfg::kAccF16 && wi.splits > 1;
+      const bool split = !Cfg::kAccF16 && !kSplitK && wi.splits > 1;
+      const uint32_t red_par = static_cast<uint32_t>((acc_iter - 1) & 1);
+      if constexpr (kSplitK) {
+        if (krank != 0) {
+          if (!splitk_push(t_row, row_in_cta, red_par, tempty_bar0 + 8u * buf, wi.tile)) break;
+          continue;  // rank 0 stores the tile
+        }
+        if (!splitk_wait_partials(red_par, wi.tile)) break;
+      }
       if (split) {
         // Stream-K tail tile shared with other units.  (a) Park this unit's
         // partial accumulator (fp32) in its workspace slot and give the TMEM
@@ -959,7 +1091,31 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             ptx::mbar_arrive(tempty_bar0 + 8u * buf);
         }
       };
-      if (split) {
+      if constexpr (kSplitK) {
+        // Rank 0: its own accumulator plus the other ranks' partials, in
+        // rank order.
+#pragma unroll 1
+        for (int c = 0; c < Cfg::kBN / 64; ++c) {
+          uint32_t v0[32], v1[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c * 64, v0);
+          ptx::tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
+          ptx::tmem_wait_ld(v0);
+          ptx::tmem_regs_ready(v1);
+          float acc[64];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            acc[i] = __uint_as_float(v0[i]);
+            acc[32 + i] = __uint_as_float(v1[i]);
+          }
+          if (c == Cfg::kBN / 64 - 1) release_tmem();
+          splitk_add(acc, c * 64, 64, row_in_cta);
+          if (c == Cfg::kBN / 64 - 1) splitk_release_slots();
+          uint32_t packed[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) packed[i] = pack_half2(acc[2 * i], acc[2 * i + 1]);
+          store_chunk(packed, c);
+        }
+      } else if (split) {
 #pragma unroll 1
         for (int c = 0; c < Cfg::kBN / 64; ++c) {
           // (c) The tile's value: the contributors' partials summed in unit
@@ -1028,8 +1184,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   }
 
   ptx::tc_fence_before();
-  if constexpr (kPair)
-    ptx::cluster_sync();  // no CTA leaves while its peer may still touch its memory
+  if constexpr (kClustered)
+    ptx::cluster_sync();  // no CTA leaves while another may still touch its memory
   else
     __syncthreads();
   if (warp == 1) {

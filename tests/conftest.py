@@ -82,10 +82,13 @@ def assert_close(got, ref, acc, what=""):
 # library by test_abi_host.py::test_variant_table).
 VARIANTS = ["tc_pair_256x256_s6", "tc_single_128x256_s4", "tc_pair_256x128_s8",
             "tc_single_128x64_s8", "tc_swap_16x128_s11", "tc_swap_32x128_s10",
-            "tc_swap_64x128_s8", "tc_pair_mc_256x256_s6"]
+            "tc_swap_64x128_s8", "tc_pair_mc_256x256_s6", "tc_swap_16x128_k2",
+            "tc_swap_32x128_k2", "tc_swap_64x128_k2", "tc_single_128x64_k4"]
 # The variants built for large M (the swapped-roles ones, made for a few rows
 # of C, would take minutes on the full-size squares).
-VARIANTS_WIDE = VARIANTS[:4] + VARIANTS[7:]
+VARIANTS_WIDE = [v for v in VARIANTS if "swap" not in v]
+# Split-K clusters: the CTAs of a cluster share each tile, one k-slice each.
+VARIANTS_SPLITK = [v for v in VARIANTS if v.endswith(("_k2", "_k4"))]
 
 
 @pytest.fixture(scope="session")

@@ -78,11 +78,16 @@ def test_auto_schedule_uses_the_tail_on_quantized_waves(plan):
 def test_auto_schedule_swapped_roles(plan):
     """Few tall tiles (C with at most 64 rows): each tile is cut into the
     same whole number of k-pieces when its partial tiles are large or there
-    are pieces to spare, else the units' ranges run on across tiles."""
+    are pieces to spare, else the units' ranges run on across tiles.  Two
+    pieces per tile run as split-K clusters of two CTAs (the partial goes
+    through shared memory); more pieces through the stream-K share."""
     d = plan.describe(64, 8192, 8192)         # 64 tiles of 128 columns: 2 pieces each
-    assert d["variant"] == "tc_swap_64x128_s8" and d["sk_units"] == 128 and d["dp_tiles"] == 0
+    assert d["variant"] == "tc_swap_64x128_k2" and d["sk_units"] == 0
+    assert d["units"] == 64 and d["grid_ctas"] == 128 and d["dp_tiles"] == 64
     d = plan.describe(16, 8192, 8192)         # 2 x 64 tiles <= 152 units: 2 pieces each
-    assert d["sk_units"] == 128
+    assert d["variant"] == "tc_swap_16x128_k2" and d["grid_ctas"] == 128
+    d = plan.describe(64, 4096, 8192)         # 32 tiles: 4 pieces each, stream-K share
+    assert d["variant"] == "tc_swap_64x128_s8" and d["sk_units"] == 128
     d = plan.describe(48, 12288, 8192)        # 96 tiles, one piece each: whole tiles
     assert d["sk_units"] == 0 and d["units"] == 96 and d["dp_tiles"] == 96
     d = plan.describe(16, 16384, 16384)       # 128 tiles of 16 rows: ranges over all units
