@@ -697,6 +697,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                              (args.b_mn ? ptx::kIdescBMnMajor : 0u);
       const uint64_t a_kstep = args.a_mn ? 128u : 2u;
       const uint64_t b_kstep = args.b_mn ? 128u : 2u;
+      // Stage 0's descriptors; stage s differs only in the start-address
+      // field (address / 16, 14 bits: shared memory stays below 256 KB), so
+      // it is stage 0's plus s stages' bytes / 16.  The issue loop is on the
+      // tensor pipe's critical path: every instruction saved there counts.
+      const uint64_t a_desc0 =
+          args.a_mn ? ptx::sw128_mnmajor_desc(sA(0)) : ptx::sw128_kmajor_desc(sA(0));
+      const uint64_t b_desc0 =
+          args.b_mn ? ptx::sw128_mnmajor_desc(sB(0)) : ptx::sw128_kmajor_desc(sB(0));
+      constexpr uint64_t kADescStage = Cfg::kABytes >> 4;
+      constexpr uint64_t kBDescStage = Cfg::kBBytes >> 4;
       Sched sched(args, unit, units, ring, static_cast<int32_t>(krank), Cfg::kSplit);
       WorkItem wi;
       int stage = 0;
@@ -718,24 +728,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint64_t a_desc = args.a_mn ? ptx::sw128_mnmajor_desc(sA(stage))
-                                            : ptx::sw128_kmajor_desc(sA(stage));
-          const uint64_t b_desc = args.b_mn ? ptx::sw128_mnmajor_desc(sB(stage))
-                                            : ptx::sw128_kmajor_desc(sB(stage));
-          // K steps holding data: all four, except in a last k-block cut by
-          // K, whose steps past K multiply the zeros the TMA filled in.
-          const int32_t k_steps = kb == args.num_kb - 1 ? (args.K - kb * Cfg::kBK + 15) / 16
-                                                        : Cfg::kBK / 16;
+          const uint64_t a_desc = a_desc0 + kADescStage * static_cast<uint32_t>(stage);
+          const uint64_t b_desc = b_desc0 + kBDescStage * static_cast<uint32_t>(stage);
+          const uint32_t acc_first = kb != wi.kb0 ? 1u : 0u;
           if (ptx::elect_one()) {
 #pragma unroll
             for (int k = 0; k < Cfg::kBK / 16; ++k) {
               // One 16-deep K step: +32 bytes inside the swizzled row
               // (K-major) or +16 K-rows = 2048 bytes (MN-major); descriptors
               // count in 16 B.  The first step of the item overwrites the
-              // accumulator.
-              if (k < k_steps)
-                ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + a_kstep * k, b_desc + b_kstep * k,
-                                         idesc, (kb != wi.kb0 || k != 0) ? 1u : 0u);
+              // accumulator.  (Steps past K in a last k-block cut by K
+              // multiply the zeros the TMA filled in; skipping them measured
+              // 2% slower, the issue loop being on the critical path.)
+              ptx::mma_f16<Cfg::kCtas>(d_tmem, a_desc + a_kstep * k, b_desc + b_kstep * k, idesc,
+                                       k != 0 ? 1u : acc_first);
             }
             // The stage is free once every pair reading it is done: with
             // multicast every pair's issuer releases it in every CTA of the
