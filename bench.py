@@ -314,6 +314,7 @@ class Setup:
         plan.set_tile_order(args.tile_order)
         plan.set_schedule(args.schedule)
         plan.set_pdl(args.pdl == "on")
+        plan.set_clock_record(True)
         self.w = w = resolve_workload(args)
         self.acc = args.acc
         self.a_np, self.b_np = wl.inputs_for(w)

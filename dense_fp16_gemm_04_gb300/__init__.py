@@ -96,6 +96,7 @@ def load():
                                              ctypes.POINTER(i32)]),
             "gemm_plan_launch_count": (u64, [vp]),
             "gemm_plan_kernel_clock": (st, [vp, ctypes.POINTER(u64)]),
+            "gemm_plan_set_clock_record": (st, [vp, i32]),
             "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "gemm_version": (ctypes.c_char_p, []),
         }
@@ -270,6 +271,11 @@ class Plan:
         out = (ctypes.c_int32 * 3)()
         _check(self._lib.gemm_plan_resident_units(self._h, out), "gemm_plan_resident_units")
         return {"ctas": out[0], "pairs": out[1], "quads": out[2]}
+
+    def set_clock_record(self, enable: bool) -> None:
+        """Kernels add to the plan's clock record (off by default)."""
+        _check(self._lib.gemm_plan_set_clock_record(self._h, 1 if enable else 0),
+               "gemm_plan_set_clock_record")
 
     def kernel_clock(self) -> dict:
         """Synchronize, then read and reset the kernels' own clock record:

@@ -139,6 +139,7 @@ struct gemm_plan_s {
   int32_t skip_kb = -1;
   int32_t forced_variant = -1;
   bool pdl = true;  // programmatic dependent launch of the GEMM kernel
+  bool clock_record = false;  // kernels add to the clock record (gemm_plan_set_clock_record)
   uint64_t launches = 0;
   uint64_t clock = 0;
   MapEntry maps[kMapCacheSize];
@@ -540,7 +541,7 @@ gemm_status_t run_device(gemm_plan_s* p, const void* A, const void* B, void* C, 
   args.sk_ws = p->sk_ws;
   args.sk_count = p->sk_count;
   args.tile_ctr = sch.dyn ? p->tile_ctr : nullptr;
-  args.clk = p->d_clk;
+  args.clk = p->clock_record ? p->d_clk : nullptr;
 
   const bool f32 = acc == GEMM_ACC_F32;
   cudaError_t e;
@@ -794,6 +795,12 @@ int32_t gemm_plan_describe(gemm_plan_t p, int64_t M, int64_t N, int64_t K, gemm_
 gemm_status_t gemm_plan_set_tile_order(gemm_plan_t p, int32_t mode) {
   if (!p || mode < 0 || mode > 2) return GEMM_ERR_INVALID_ARG;
   p->tile_order = mode;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_clock_record(gemm_plan_t p, int32_t enable) {
+  if (!p || (enable != 0 && enable != 1)) return GEMM_ERR_INVALID_ARG;
+  p->clock_record = enable != 0;
   return GEMM_OK;
 }
 

@@ -149,17 +149,24 @@ GEMM_API gemm_status_t gemm_plan_check_error(gemm_plan_t plan);
  * WaitSite list), detail[2] = CTA index, detail[3] = tile index. */
 GEMM_API gemm_status_t gemm_plan_last_error_detail(gemm_plan_t plan, uint32_t detail[4]);
 
-/* The SM clock the kernels actually ran at.  Every GEMM kernel launched
- * through the plan has its first CTA add 1, its lifetime in SM cycles
- * (%clock64) and its lifetime in nanoseconds (%globaltimer) to a device
- * record; this call synchronizes the device, copies the record to
- * out[0] = launches, out[1] = cycles, out[2] = ns, and sets it back to
- * zero.  out[1] * 1000 / out[2] is the mean SM clock in MHz over those
+/* The SM clock the kernels actually ran at.  While the plan's clock record
+ * is on (gemm_plan_set_clock_record), every GEMM kernel launched through the
+ * plan has its first CTA add 1, its lifetime in SM cycles (%clock64) and its
+ * lifetime in nanoseconds (%globaltimer) to a device record; this call
+ * synchronizes the device, copies the record to out[0] = launches,
+ * out[1] = cycles, out[2] = ns, and sets it back to zero.  out[1] * 1000 / out[2] is the mean SM clock in MHz over those
  * launches (a clock sampled from outside, e.g. by NVML, can miss the drop a
  * power-capped kernel causes).  gemm_run_host's launches count too; the
  * K == 0 zero-fill does not.  No counterpart in the source pages (a
  * measurement aid). */
 GEMM_API gemm_status_t gemm_plan_kernel_clock(gemm_plan_t plan, uint64_t out[3]);
+
+/* Clock record on (1) or off (0, the default).  The record's three atomics
+ * at the end of the first CTA lengthen a launch of a few microseconds by
+ * ~0.15 us (512^3 in a CUDA graph: 4.30 vs 4.15 us per GEMM); measurement
+ * turns it on.  GEMM_ERR_INVALID_ARG for other values.  No counterpart in
+ * the source pages (a measurement aid). */
+GEMM_API gemm_status_t gemm_plan_set_clock_record(gemm_plan_t plan, int32_t enable);
 
 /* Watchdog and fault-injection controls (testing and diagnosis).
  * timeout_ns: how long any one wait inside the kernel may take before it

@@ -77,22 +77,32 @@ def test_memory_of_no_device_or_the_host_is_refused(plan):
     assert bool((c == 3.0).all())
 
 
-def test_kernel_clock_record(plan):
-    """Each GEMM launch adds one to the kernel's clock record, with CTA 0's
-    lifetime in SM cycles and ns: their ratio is an SM clock the part can
-    run at, and reading the record clears it."""
+def test_kernel_clock_record():
+    """With the clock record on, each GEMM launch adds one to it, with CTA
+    0's lifetime in SM cycles and ns: their ratio is an SM clock the part
+    can run at, and reading the record clears it.  Off (the default), the
+    kernels leave it alone."""
+    p = g.Plan(0)
     M = N = K = 1024
     a, b = wl.draw(M, N, K, seed=33)
     ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
     c = torch.empty((M, N), dtype=torch.float16, device="cuda")
-    plan.kernel_clock()
+    for _ in range(3):
+        p.run(ta, tb, c)
+    assert p.kernel_clock()["launches"] == 0
+    p.set_clock_record(True)
     for _ in range(5):
-        plan.run(ta, tb, c)
-    r = plan.kernel_clock()
+        p.run(ta, tb, c)
+    r = p.kernel_clock()
     assert r["launches"] == 5 and r["cycles"] > 0 and r["ns"] > 0
     assert 200.0 < r["mhz"] < 3000.0, r
-    assert plan.kernel_clock()["launches"] == 0
-    plan.check_error()
+    assert p.kernel_clock()["launches"] == 0
+    p.set_clock_record(False)
+    p.run(ta, tb, c)
+    assert p.kernel_clock()["launches"] == 0
+    assert p._lib.gemm_plan_set_clock_record(p._h, 2) == INVALID
+    p.check_error()
+    p.close()
 
 
 def test_writes_stay_inside_C(plan):
