@@ -18,17 +18,21 @@
 //                       where every TMA row straddles two L2 lines);
 //   kSwap               roles swapped for C with few rows: the MMA's M runs
 //                       over 128 columns of C (rows of B) and its N over
-//                       kBN = 16..64 rows of C, and the epilogue writes the
-//                       transposed tile straight to C;
+//                       kBN = 16..64 rows of C, and the epilogue transposes
+//                       8 x 8 blocks in registers and writes C straight from
+//                       them, 16 bytes per lane;
 //   kSplit = 2 or 4     a cluster of single CTAs (plain or swapped roles)
 //                       shares every tile it is given, each CTA accumulating
-//                       one k-slice; the CTAs of rank > 0 write their fp32
-//                       partial tiles into rank 0's shared memory
-//                       (st.shared::cluster, one release arrival per thread)
-//                       and rank 0 adds them to its own, in rank order, and
-//                       stores the tile -- for problems of few tiles with many
+//                       one k-slice, and the partial tiles meet in shared
+//                       memory (st.shared::cluster, one release arrival per
+//                       thread) -- for problems of few tiles with many
 //                       k-blocks each, without a round trip through global
-//                       memory.
+//                       memory.  Plain roles: the CTAs of rank > 0 write
+//                       their fp32 partials into rank 0's shared memory and
+//                       rank 0 adds them to its own, in rank order, and stores
+//                       the tile.  Swapped roles (kSplit = 2): each CTA
+//                       finishes half of the tile's rows of C and sends the
+//                       other half of its partial to the other CTA.
 // Operands are K-contiguous or M/N-contiguous (run-time choice: TMA box shape,
 // shared-memory descriptor and the instruction descriptor's transpose bits).
 //
@@ -267,6 +271,13 @@ struct Sched {
   __device__ __forceinline__ int32_t slot_of(int32_t u, int32_t t) const {
     return static_cast<int32_t>(bound(u) / num_kb) == t ? 0 : 1;
   }
+  // Whether next() may hand out another item (with the dynamic order, whose
+  // next tile is not known yet, always true once the first whole tile is out).
+  __device__ __forceinline__ bool has_more() const {
+    if (x < x_end) return true;
+    if (dyn && first_done) return true;
+    return next_dp < dp_tiles;
+  }
   // Stream-K pieces come first and whole tiles after them: the fix-up of a
   // shared tile (reading the other units' partials) then overlaps the main
   // loop of a later whole tile instead of ending the kernel.
@@ -313,9 +324,11 @@ struct GemmCfg {
   static constexpr int kMc = kMc_;
   static constexpr int kPairs = kMc;  // CTA pairs (or lone CTAs) per cluster
   // kSplit > 1: a cluster of kSplit single CTAs shares every tile it is
-  // given, each CTA accumulating its own k-slice; the CTAs of rank > 0 write
-  // their fp32 partial tiles into the shared memory of rank 0, which adds
-  // them to its own (in rank order) and stores the tile.
+  // given, each CTA accumulating its own k-slice.  Plain roles: the CTAs of
+  // rank > 0 write their fp32 partial tiles into the shared memory of rank 0,
+  // which adds them to its own (in rank order) and stores the tile.  Swapped
+  // roles (kSplit = 2): rank r finishes accumulator columns [r kBN/2,
+  // (r+1) kBN/2) (rows of C) and receives the other rank's partial of them.
   static constexpr int kSplit = kSplit_;
   static constexpr int kClusterCtas = kCtas * kPairs * kSplit;
   // Swapped roles (for small M): the MMA's "A" operand is a 128-row tile of B
@@ -335,9 +348,11 @@ struct GemmCfg {
   static constexpr int kEpiWarps = 4;
   static constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 fp16, 128B swizzle
   static constexpr int kEpiBytes = kSwap ? 0 : kEpiWarps * 2 * kEpiBufBytes;
-  // Split-K: kSplit - 1 partial tiles of 128 x kBN fp32 received by rank 0,
-  // each stored [column / 4][row][column % 4].
-  static constexpr int kRedBytes = (kSplit - 1) * kBM * kBN * 4;
+  // Split-K: the fp32 partials a CTA receives, each stored
+  // [column / 4][row][column % 4]: kSplit - 1 whole 128 x kBN tiles (rank 0,
+  // plain roles) or one 128 x kBN/2 half (every rank, swapped roles).
+  static constexpr int kRedBytes = kSwap ? (kSplit - 1) * kBM * (kBN / kSplit) * 4
+                                         : (kSplit - 1) * kBM * kBN * 4;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kStages * kABytes;
   static constexpr int kOffEpi = kStages * kStageBytes;
@@ -367,6 +382,7 @@ struct GemmCfg {
   static_assert(kClusterCtas <= 8, "portable cluster size");
   static_assert(kSplit == 1 || ((kSplit == 2 || kSplit == 4) && kCtas == 1 && kMc == 1 && !kAccF16),
                 "split-K clusters: 2 or 4 single CTAs, fp32 partials");
+  static_assert(!kSwap || kSplit <= 2, "swapped roles split K in two (a half tile per CTA)");
   static_assert(kSwap ? (kCtas == 1 && (kBN == 16 || kBN == 32 || kBN == 64))
                       : (kBN == 64 || kBN == 128 || kBN == 256),
                 "tile width: 64, 128 or 256; 16, 32 or 64 with swapped roles (one CTA)");
@@ -398,6 +414,69 @@ __device__ __forceinline__ void raster(int32_t t, int32_t tiles_m, int32_t tiles
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// kCols consecutive fp32 accumulator columns of this thread's TMEM lane
+// (32x32b loads: thread t of the warp reads lane base + t), one wait for all.
+template <int kCols>
+__device__ __forceinline__ void tmem_ld_f32(uint32_t taddr, float* out) {
+  static_assert(kCols % 8 == 0, "columns come in groups of eight");
+  uint32_t v[kCols];
+#pragma unroll
+  for (int g = 0; g < kCols / 16; ++g)
+    ptx::tmem_ld_32x32b_x16(taddr + g * 16, *reinterpret_cast<uint32_t(*)[16]>(v + g * 16));
+  if constexpr (kCols % 16 != 0)
+    ptx::tmem_ld_32x32b_x8(taddr + kCols / 16 * 16,
+                           *reinterpret_cast<uint32_t(*)[8]>(v + kCols / 16 * 16));
+  ptx::tmem_wait_ld(v);
+#pragma unroll
+  for (int i = 0; i < kCols; ++i) out[i] = __uint_as_float(v[i]);
+}
+
+// Store kRows rows of a swapped-roles tile of C.  Lane l of the warp holds
+// column n_lane of C (the lanes' columns consecutive, the first a multiple
+// of 8) and in v[i] the value of row m0 + i.  Within each group of eight
+// lanes, every 8 x 8 block (eight rows, the group's eight columns) is
+// transposed in registers by a three-step butterfly: at distance d = 4, 2, 1
+// a lane swaps with lane ^ d the four values whose index differs from its
+// own lane index in bit d.  After it lane (g, j) holds row 8b + j, columns
+// 8g .. 8g + 7 of the warp's 32, rounded to fp16 and written as one 16-byte
+// store: per row the warp's four groups write 64 contiguous bytes, instead
+// of one 2-byte store per lane per row.  Rows at or past M and column groups
+// at or past N (N is a multiple of 8) are not written; every lane takes
+// part in the shuffles.
+template <int kRows>
+__device__ __forceinline__ void store_swapped_rows(const float* v, uint16_t* C, int64_t ldc,
+                                                   int32_t M, int32_t N, int32_t m0,
+                                                   int32_t n_lane, int lane) {
+  static_assert(kRows % 8 == 0, "rows come in blocks of eight");
+  const int j = lane & 7;
+  const int32_t n = n_lane - j;  // first of this lane group's eight columns
+#pragma unroll
+  for (int b = 0; b < kRows / 8; ++b) {
+    float x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = v[8 * b + k];
+#pragma unroll
+    for (int d = 4; d >= 1; d >>= 1) {
+      const bool upper = (j & d) != 0;
+#pragma unroll
+      for (int k0 = 0; k0 < 8; ++k0) {
+        if (k0 & d) continue;
+        const int k1 = k0 | d;
+        const float out = upper ? x[k0] : x[k1];
+        const float in = __shfl_xor_sync(0xffffffffu, out, d);
+        if (upper)
+          x[k0] = in;
+        else
+          x[k1] = in;
+      }
+    }
+    const int32_t m = m0 + 8 * b + j;
+    if (m < M && n < N)
+      ptx::st_global_v4(C + static_cast<size_t>(m) * ldc + n, pack_half2(x[0], x[1]),
+                        pack_half2(x[2], x[3]), pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+  }
 }
 
 template <class Cfg>
@@ -455,7 +534,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                       warp == 0 && rank == 0 ? bar_tile_took : 0u};
   // Split-K partial tiles in rank 0: slot r - 1 for rank r, element (TMEM
   // lane l, column c) at ((c / 4) * 128 + l) * 16 + (c % 4) * 4 bytes, so a
-  // warp's 32 lanes move 512 contiguous bytes per 16-byte access.
+  // warp's 32 lanes move 512 contiguous bytes per 16-byte access.  (Swapped
+  // roles: one slot in every rank, for the half of the columns it finishes.)
   constexpr uint32_t kRedSlotBytes = static_cast<uint32_t>(Cfg::kBM * Cfg::kBN * 4);
   // Epilogue warps of a split-K CTA: rank > 0 writes its accumulator (TMEM
   // buffer at t_row, this thread's lane `lrow`) into its slot of rank 0
@@ -537,10 +617,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
     ptx::mbar_init(bar_tile_took, 1);  // the leader's A producer read a tile
     if constexpr (kSplitK) {
-      // One arrival per epilogue thread of every other rank (each releases
-      // its own partial-tile stores), and one per epilogue thread of rank 0
-      // (each has read its rows of the slot).
-      ptx::mbar_init(bar_red_full, 32 * Cfg::kEpiWarps * (Cfg::kSplit - 1));
+      // red_full, plain roles: one arrival per epilogue thread of every rank
+      // that sends to rank 0 (each releases its own partial-tile stores);
+      // swapped roles: this CTA's own arrival with the expected byte count,
+      // which the other rank's asynchronous stores complete.  red_empty: one
+      // arrival per epilogue thread of the rank this one sends to (each has
+      // read its rows of the slot) -- rank 0 (plain roles) or the other rank
+      // (swapped roles).
+      ptx::mbar_init(bar_red_full, Cfg::kSwap ? 1 : 32 * Cfg::kEpiWarps * (Cfg::kSplit - 1));
       ptx::mbar_init(bar_red_empty, 32 * Cfg::kEpiWarps);
     }
     *abort_flag = 0u;
@@ -836,9 +920,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     // ---------------------------------------------- epilogue, swapped roles --
     ptx::griddep_wait();  // writes C and the workspace
     // The MMA computed a tile of C^T = B x A^T: TMEM lane = column n of C,
-    // TMEM column = row m of C.  Each thread owns one column n and stores its
-    // kBN values down it; for a fixed m the warp's 32 lanes write 32
-    // consecutive columns, 64 contiguous bytes per store.
+    // TMEM column = row m of C.  Each thread owns one column n and holds its
+    // kBN values down it; store_swapped_rows turns them around in registers
+    // so that each lane writes 8 columns of one row at a time.
     const int q = warp & 3;  // this warp may touch TMEM lanes 32q .. 32q+31 only
     const int row_in_cta = q * 32 + lane;
     const uint32_t tempty_bar0 = bar_tempty(0);
@@ -869,25 +953,65 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const bool split = !Cfg::kAccF16 && !kSplitK && wi.splits > 1;
       float acc[Cfg::kBN];
       if constexpr (kSplitK) {
+        // Rank r finishes rows m0 + r H .. m0 + (r + 1) H - 1 of C
+        // (accumulator columns r H .., H = kBN / 2): it sends its partial of
+        // the other half to the other rank, keeps its own half and adds the
+        // other rank's partial of it.  A sum of two terms: which rank adds
+        // does not change the result.  Slot layout as above, for H columns.
+        constexpr int kHalf = Cfg::kBN / 2;
+        constexpr uint32_t kHalfBytes = static_cast<uint32_t>(Cfg::kBM * kHalf * 4);
         const uint32_t red_par = static_cast<uint32_t>((acc_iter - 1) & 1);
-        if (krank != 0) {
-          if (!splitk_push(t_row, row_in_cta, red_par, tempty_bar0 + 8u * buf, wi.tile)) break;
-          continue;  // rank 0 stores the tile
-        }
-        if (!splitk_wait_partials(red_par, wi.tile)) break;
+        const uint32_t peer = krank ^ 1u;
+        // (a) Arm this CTA's red_full for the other rank's half of this tile
+        // (its stores may land before or after), and wait until the other
+        // rank has read what this one sent it for the previous tile.
+        if (threadIdx.x == 64) ptx::mbar_arrive_expect_tx(bar_red_full, kHalfBytes);
+        if (lane == 0)
+          ok = wait_bar<true>(bar_red_empty, red_par ^ 1u, w, kSiteRedEmpty, wi.tile) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ptx::named_barrier_and(1, 32 * Cfg::kEpiWarps, ok != 0)) break;
+        // (b) Send the other rank's half: asynchronous stores that count
+        // themselves on its red_full, so this thread does not wait for them.
+        {
+          float part[kHalf];
+          tmem_ld_f32<kHalf>(t_row + peer * kHalf, part);
+          const uint32_t dst =
+              ptx::mapa(sb + Cfg::kOffRed, peer) + static_cast<uint32_t>(row_in_cta) * 16u;
+          const uint32_t peer_full = ptx::mapa(bar_red_full, peer);
 #pragma unroll
-        for (int g = 0; g < Cfg::kBN / 16; ++g) {
-          uint32_t v[16];
-          ptx::tmem_ld_32x32b_x16(t_row + g * 16, v);
-          ptx::tmem_wait_ld(v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) acc[g * 16 + i] = __uint_as_float(v[i]);
+          for (int c4 = 0; c4 < kHalf / 4; ++c4)
+            ptx::st_async_cluster_v4(dst + static_cast<uint32_t>(c4 * Cfg::kBM) * 16u,
+                                     __float_as_uint(part[4 * c4]),
+                                     __float_as_uint(part[4 * c4 + 1]),
+                                     __float_as_uint(part[4 * c4 + 2]),
+                                     __float_as_uint(part[4 * c4 + 3]), peer_full);
         }
+        // (c) Own half into registers; the TMEM buffer goes back to the MMA
+        // issuer.
+        tmem_ld_f32<kHalf>(t_row + krank * kHalf, acc);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(tempty_bar0 + 8u * buf);
-        splitk_add(acc, 0, Cfg::kBN, row_in_cta);
-        splitk_release_slots();
+        // (d) Add the other rank's partial of this half, free the slot (not
+        // after the unit's last tile: nothing more is sent), store.
+        if (!splitk_wait_partials(red_par, wi.tile)) break;
+        const uint32_t src = sb + Cfg::kOffRed + static_cast<uint32_t>(row_in_cta) * 16u;
+        uint32_t read = 0;  // depends on every value read from the slot
+#pragma unroll
+        for (int c4 = 0; c4 < kHalf / 4; ++c4) {
+          const float4 p = ptx::ld_shared_v4_f32(src + static_cast<uint32_t>(c4 * Cfg::kBM) * 16u);
+          acc[4 * c4] += p.x;
+          acc[4 * c4 + 1] += p.y;
+          acc[4 * c4 + 2] += p.z;
+          acc[4 * c4 + 3] += p.w;
+          read ^= __float_as_uint(p.x) ^ __float_as_uint(p.y) ^ __float_as_uint(p.z) ^
+                  __float_as_uint(p.w);
+        }
+        if (sched.has_more())
+          ptx::mbar_arrive_relaxed_cluster_after(ptx::mapa(bar_red_empty, peer), read);
+        store_swapped_rows<kHalf>(acc, args.C, args.ldc, args.M, args.N,
+                                  m0 + static_cast<int32_t>(krank) * kHalf, n, lane);
+        continue;
       } else if (split) {
         // Same protocol as the plain epilogue: park the fp32 partial, count,
         // and the last contributor sums all partials in unit order.
@@ -958,18 +1082,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(tempty_bar0 + 8u * buf);
       }
-      if (n < args.N) {
-        uint16_t* col = args.C + n;
-#pragma unroll
-        for (int i = 0; i < Cfg::kBN; ++i) {
-          const int32_t m = m0 + i;
-          if (m < args.M) {
-            const __half h = __float2half_rn(acc[i]);
-            ptx::st_global_b16(col + static_cast<size_t>(m) * args.ldc,
-                               *reinterpret_cast<const uint16_t*>(&h));
-          }
-        }
-      }
+      store_swapped_rows<Cfg::kBN>(acc, args.C, args.ldc, args.M, args.N, m0, n, lane);
     }
   } else {
     // ------------------------------------------------------------ epilogue --
@@ -1115,7 +1228,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           }
           if (c == Cfg::kBN / 64 - 1) release_tmem();
           splitk_add(acc, c * 64, 64, row_in_cta);
-          if (c == Cfg::kBN / 64 - 1) splitk_release_slots();
+          // Nothing more is sent after the unit's last tile.
+          if (c == Cfg::kBN / 64 - 1 && sched.has_more()) splitk_release_slots();
           uint32_t packed[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) packed[i] = pack_half2(acc[2 * i], acc[2 * i + 1]);
