@@ -527,6 +527,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   auto sB = [&](int s) { return sb + Cfg::kOffB + s * Cfg::kBBytes; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
   const Watch w{abort_flag, args.err, args.timeout_ns};
+  // Swapped-roles split-K, thread 64: parity + 1 of a red_full phase armed
+  // for the other rank's partial and not yet seen complete (0: none).
+  uint32_t red_pending = 0;
   // The dynamic tile order as every role reads it (tile_empty lives in the
   // cluster's leader, rank 0, where the scheduler runs).
   const TileRing ring{sb + Cfg::kOffTiles, bar_tile_full(0),
@@ -965,7 +968,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         // (a) Arm this CTA's red_full for the other rank's half of this tile
         // (its stores may land before or after), and wait until the other
         // rank has read what this one sent it for the previous tile.
-        if (threadIdx.x == 64) ptx::mbar_arrive_expect_tx(bar_red_full, kHalfBytes);
+        if (threadIdx.x == 64) {
+          ptx::mbar_arrive_expect_tx(bar_red_full, kHalfBytes);
+          red_pending = red_par + 1u;
+        }
         if (lane == 0)
           ok = wait_bar<true>(bar_red_empty, red_par ^ 1u, w, kSiteRedEmpty, wi.tile) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -995,6 +1001,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         // (d) Add the other rank's partial of this half, free the slot (not
         // after the unit's last tile: nothing more is sent), store.
         if (!splitk_wait_partials(red_par, wi.tile)) break;
+        red_pending = 0;
         const uint32_t src = sb + Cfg::kOffRed + static_cast<uint32_t>(row_in_cta) * 16u;
         uint32_t read = 0;  // depends on every value read from the slot
 #pragma unroll
@@ -1304,10 +1311,27 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   }
 
   ptx::tc_fence_before();
-  if constexpr (kClustered)
+  if constexpr (kSplitK) {
+    // No CTA leaves while another may still touch its memory.  In a split-K
+    // cluster every such access (a partial tile, an arrival on red_full or
+    // red_empty) is waited for by the CTA it targets before that CTA gets
+    // here, unless a wait gave up: then a swapped-roles CTA first waits
+    // (bounded) for the partial it armed red_full for, and the cluster
+    // barrier releases and acquires.  Otherwise it need not order memory;
+    // a release arrival would wait for this thread's stores of C to
+    // complete (~0.45 us at the end of every launch).
+    if (threadIdx.x == 64 && red_pending != 0u && *abort_flag != 0u)
+      wait_bar<true>(bar_red_full, red_pending - 1u, w, kSiteRedFull, -1, false);
+    __syncthreads();  // after it every thread reads the same abort flag
+    if (*abort_flag != 0u)
+      ptx::cluster_sync();
+    else
+      ptx::cluster_sync_relaxed();
+  } else if constexpr (kClustered) {
     ptx::cluster_sync();  // no CTA leaves while another may still touch its memory
-  else
+  } else {
     __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc<Cfg::kCtas>(tmem_base, Cfg::kTmemCols);

@@ -206,6 +206,14 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// Cluster barrier that only brings the CTAs together: the relaxed arrival
+// orders none of this thread's earlier memory accesses, so it does not wait
+// for its global stores to complete as a release arrival does.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::
+                   : "memory");
+}
+
 // --------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
