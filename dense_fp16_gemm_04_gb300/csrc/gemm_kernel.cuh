@@ -439,43 +439,51 @@ __device__ __forceinline__ void tmem_ld_f32(uint32_t taddr, float* out) {
 // lanes, every 8 x 8 block (eight rows, the group's eight columns) is
 // transposed in registers by a three-step butterfly: at distance d = 4, 2, 1
 // a lane swaps with lane ^ d the four values whose index differs from its
-// own lane index in bit d.  After it lane (g, j) holds row 8b + j, columns
-// 8g .. 8g + 7 of the warp's 32, rounded to fp16 and written as one 16-byte
-// store: per row the warp's four groups write 64 contiguous bytes, instead
-// of one 2-byte store per lane per row.  Rows at or past M and column groups
-// at or past N (N is a multiple of 8) are not written; every lane takes
-// part in the shuffles.
+// own lane index in bit d.  Each step runs over all blocks before the next,
+// so its shuffles are independent and issue back to back.  After it lane
+// (g, j) holds row 8b + j, columns 8g .. 8g + 7 of the warp's 32, rounded to
+// fp16 and written as one 16-byte store: per row the warp's four groups
+// write 64 contiguous bytes, instead of one 2-byte store per lane per row.
+// Rows at or past M and column groups at or past N (N is a multiple of 8)
+// are not written; every lane takes part in the shuffles.
 template <int kRows>
 __device__ __forceinline__ void store_swapped_rows(const float* v, uint16_t* C, int64_t ldc,
                                                    int32_t M, int32_t N, int32_t m0,
                                                    int32_t n_lane, int lane) {
   static_assert(kRows % 8 == 0, "rows come in blocks of eight");
+  constexpr int kBlocks = kRows / 8;
   const int j = lane & 7;
   const int32_t n = n_lane - j;  // first of this lane group's eight columns
+  float x[kBlocks][8];
 #pragma unroll
-  for (int b = 0; b < kRows / 8; ++b) {
-    float x[8];
+  for (int b = 0; b < kBlocks; ++b)
 #pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] = v[8 * b + k];
+    for (int k = 0; k < 8; ++k) x[b][k] = v[8 * b + k];
 #pragma unroll
-    for (int d = 4; d >= 1; d >>= 1) {
-      const bool upper = (j & d) != 0;
+  for (int d = 4; d >= 1; d >>= 1) {
+    const bool upper = (j & d) != 0;
+#pragma unroll
+    for (int b = 0; b < kBlocks; ++b) {
 #pragma unroll
       for (int k0 = 0; k0 < 8; ++k0) {
         if (k0 & d) continue;
         const int k1 = k0 | d;
-        const float out = upper ? x[k0] : x[k1];
+        const float out = upper ? x[b][k0] : x[b][k1];
         const float in = __shfl_xor_sync(0xffffffffu, out, d);
         if (upper)
-          x[k0] = in;
+          x[b][k0] = in;
         else
-          x[k1] = in;
+          x[b][k1] = in;
       }
     }
+  }
+#pragma unroll
+  for (int b = 0; b < kBlocks; ++b) {
     const int32_t m = m0 + 8 * b + j;
     if (m < M && n < N)
-      ptx::st_global_v4(C + static_cast<size_t>(m) * ldc + n, pack_half2(x[0], x[1]),
-                        pack_half2(x[2], x[3]), pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
+      ptx::st_global_v4(C + static_cast<size_t>(m) * ldc + n, pack_half2(x[b][0], x[b][1]),
+                        pack_half2(x[b][2], x[b][3]), pack_half2(x[b][4], x[b][5]),
+                        pack_half2(x[b][6], x[b][7]));
   }
 }
 
