@@ -97,7 +97,11 @@ constexpr VariantInfo kVariants[kNumVariants] = {
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s for any single wait
 constexpr size_t kRecordBytes = 64;  // watchdog record (16 B) + clock record (3 x 8 B)
 constexpr int kGroupM = 8;                             // raster group height, tiles
-constexpr int kMapCacheSize = 32;
+// Tensor-map cache: kMapSets sets of kMapWays entries (1024 maps, ~200 KB per
+// plan), so that a caller cycling through a few hundred operand buffers
+// (three maps per call) still finds every map it made.
+constexpr int kMapSets = 128;
+constexpr int kMapWays = 8;
 // gemm_run_host's pipeline: at most kHostChunksA row chunks of A and
 // kHostChunksB of B, and at most kHostBlocks blocks of C.
 constexpr int kHostChunksA = 32;
@@ -142,7 +146,7 @@ struct gemm_plan_s {
   bool clock_record = false;  // kernels add to the clock record (gemm_plan_set_clock_record)
   uint64_t launches = 0;
   uint64_t clock = 0;
-  MapEntry maps[kMapCacheSize];
+  MapEntry maps[kMapSets][kMapWays];
   // device staging for gemm_run_host
   void* dA = nullptr;
   void* dB = nullptr;
@@ -203,9 +207,15 @@ enum MapResult { kMapOk = 0, kMapNotDevice = 1, kMapEncodeFailed = 2 };
 MapResult get_map(gemm_plan_s* p, CUtensorMap* out, const void* ptr, uint64_t rows,
                   uint64_t cols, uint32_t box_rows, uint32_t box_cols, uint64_t pitch = 0) {
   if (pitch == 0) pitch = cols;
-  MapEntry* victim = &p->maps[0];
-  for (int i = 0; i < kMapCacheSize; ++i) {
-    MapEntry& e = p->maps[i];
+  // The set: a mix of the key's fields (an address, its shape and box).
+  uint64_t h = reinterpret_cast<uintptr_t>(ptr) >> 8;
+  h ^= rows * 0x9e3779b97f4a7c15ull ^ cols * 0xc2b2ae3d27d4eb4full ^ pitch * 0x165667b19e3779f9ull ^
+       (static_cast<uint64_t>(box_rows) << 32 | box_cols) * 0xd6e8feb86659fd93ull;
+  h ^= h >> 29;
+  MapEntry* set = p->maps[(h * 0xbf58476d1ce4e5b9ull >> 40) % kMapSets];
+  MapEntry* victim = &set[0];
+  for (int i = 0; i < kMapWays; ++i) {
+    MapEntry& e = set[i];
     if (e.stamp && e.ptr == ptr && e.rows == rows && e.cols == cols && e.pitch == pitch &&
         e.box_rows == box_rows && e.box_cols == box_cols) {
       e.stamp = ++p->clock;

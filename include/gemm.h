@@ -96,7 +96,7 @@ GEMM_API gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
  * tensor map it then builds), and host, managed or unregistered memory, or
  * another GPU's memory, is refused with GEMM_ERR_INVALID_ARG before any
  * launch.  (Memory freed and allocated again at the same address is not
- * looked up again while its map stays in the plan's 32-entry cache.)
+ * looked up again while its map stays in the plan's cache of 1024 maps.)
  *   A : device pointer, fp16 [M, K] row-major (K contiguous), 16-byte aligned
  *   B : device pointer, fp16 [N, K] row-major (K contiguous), 16-byte aligned
  *   C : device pointer, fp16 [M, N] row-major, 16-byte aligned, must not
