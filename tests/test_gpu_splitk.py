@@ -1,12 +1,14 @@
 """Split-K clusters (tc_swap_{16,32,64}x128_k2, tc_single_128x64_k4): the CTAs
 of a cluster share every tile they are given, each accumulating its own
-k-slice; the CTAs of rank > 0 write their fp32 partial tiles into the shared
-memory of rank 0, which adds them to its own in rank order and stores C.
+k-slice.  In tc_single_128x64_k4 the CTAs of rank > 0 write their fp32
+partial tiles into the shared memory of rank 0, which adds them to its own in
+rank order and stores C; in the swapped-roles pairs each CTA finishes half of
+the tile's rows of C and receives the other CTA's partial of them.
 
 Checked here against the CPU oracle: k-slices of unequal length (the number
 of k-blocks not a multiple of the cluster size), one k-block per CTA, ragged
 M, N and K, more tiles than resident clusters (each cluster then takes
-several tiles in turn, so rank 0 must free a partial slot before the next
+several tiles in turn, so a partial slot must be freed before the next
 tile's partial may land in it), results identical from run to run, the
 automatic choice of these variants, and fp16 accumulation falling back to
 whole tiles."""
@@ -68,8 +70,8 @@ def test_matches_oracle(variant, shape):
 
 @pytest.mark.parametrize("variant", VARIANTS_SPLITK)
 def test_more_tiles_than_clusters(variant):
-    """Every cluster takes several tiles in turn: the partial slot of rank 0
-    is reused from tile to tile."""
+    """Every cluster takes several tiles in turn: each partial slot is
+    reused from tile to tile."""
     p = _plan(variant)
     units = p.resident_units()
     M, N, K = (2048, 2048, 512) if variant == K4 else (64, 65536, 256)
