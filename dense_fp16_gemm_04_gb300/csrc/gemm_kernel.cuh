@@ -24,15 +24,17 @@
 //   kSplit = 2 or 4     a cluster of single CTAs (plain or swapped roles)
 //                       shares every tile it is given, each CTA accumulating
 //                       one k-slice, and the partial tiles meet in shared
-//                       memory (st.shared::cluster, one release arrival per
-//                       thread) -- for problems of few tiles with many
+//                       memory -- for problems of few tiles with many
 //                       k-blocks each, without a round trip through global
 //                       memory.  Plain roles: the CTAs of rank > 0 write
-//                       their fp32 partials into rank 0's shared memory and
-//                       rank 0 adds them to its own, in rank order, and stores
-//                       the tile.  Swapped roles (kSplit = 2): each CTA
-//                       finishes half of the tile's rows of C and sends the
-//                       other half of its partial to the other CTA.
+//                       their fp32 partials into rank 0's shared memory
+//                       (st.shared::cluster, one release arrival per thread)
+//                       and rank 0 adds them to its own, in rank order, and
+//                       stores the tile.  Swapped roles (kSplit = 2): each
+//                       CTA finishes half of the tile's rows of C and sends
+//                       the other half of its partial to the other CTA
+//                       (st.async, bytes completed on the receiver's
+//                       barrier).
 // Operands are K-contiguous or M/N-contiguous (run-time choice: TMA box shape,
 // shared-memory descriptor and the instruction descriptor's transpose bits).
 //
