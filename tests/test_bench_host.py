@@ -100,3 +100,28 @@ def test_clock_summary_names_every_reason():
     assert d["samples"] == 20 and d["power_w_max"] == 360.0
     s.samples = [(2070.0, 300.0, 0x1)] * 5
     assert s.summary()["reasons"] == []
+
+
+def test_kernel_source_hash_follows_code_not_comments(tmp_path, monkeypatch):
+    """A recorded ncu traffic figure is keyed by a hash of the kernel sources'
+    code: comments and whitespace leave it unchanged, a code change moves it,
+    and the committed records carry the current sources' hash."""
+    import json
+    import shutil
+    import bench
+    csrc = tmp_path / "dense_fp16_gemm_04_gb300" / "csrc"
+    shutil.copytree(os.path.join(ROOT, "dense_fp16_gemm_04_gb300", "csrc"), csrc,
+                    ignore=shutil.ignore_patterns("*.o", "*.so"))
+    h0 = bench.kernel_source_hash()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_source_hash() == h0
+    ptx = csrc / "ptx.cuh"
+    text = ptx.read_text()
+    ptx.write_text("// a comment\n" + text.replace("\n", "\n  \n", 3) + "\n/* block\n comment */\n")
+    assert bench.kernel_source_hash() == h0
+    ptx.write_text(text + "\nstatic const int kProbe = 1;\n")
+    assert bench.kernel_source_hash() != h0
+    monkeypatch.undo()
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        records = json.load(f)
+    assert records and all(r["source_hash"] == h0 for r in records.values())
